@@ -1,0 +1,212 @@
+/*
+ * moe_prefill.h -- C ABI of libmoeprefill.so: the prompt-path (prefill)
+ * routed-expert FFN of a quantized mixture-of-experts layer on one GB300
+ * (sm_103a).
+ *
+ * The layer, as the "Strata" pull requests describe it:
+ *   route   : bucket the T*k (token, expert) rows by expert -- histogram,
+ *             exclusive prefix sum, stable permutation ("Strata #3752",
+ *             commits "moe_ws wiring" and "swiglu_quant landed":
+ *             quantize_scatter and the group bounds);
+ *   q8      : activations to int8 per 32-value block, d = amax/127,
+ *             q = rint(x/d), d = 0 gives q = 0 ("Strata #3752", commit
+ *             "swiglu_quant": quantize_mmq_q8_1; the layer spec's tiny
+ *             configuration);
+ *   gate/up : per routed row, GU = sum over 32-value K blocks, in K order,
+ *             of d_w*d_x*isum, isum the exact integer block sum
+ *             ("Strata #3752", commit "moe_ws kernels");
+ *   swiglu_quant : H = silu(g)*u, requantized to q8 per 32-value block in
+ *             the same pass, H never stored ("Strata #3752", commit
+ *             "swiglu_quant");
+ *   down    : Dm = the same per-block product of the down weights with Hq;
+ *   combine : out[t] = sum over the token's top-k ranks in rank order of
+ *             w[t,r]*Dm[row(t,r)] (the layer spec's tiny configuration).
+ *
+ * Conventions for every entry point:
+ *   - Every pointer argument named d_* or documented "device" is device
+ *     memory of the current CUDA device, owned by the caller.  The library
+ *     allocates nothing and keeps no state between calls except a launch
+ *     counter; all work is enqueued on `stream` with no host
+ *     synchronisation, unless the entry point says otherwise.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     negative MOE_ERR_* code is returned and nothing is enqueued.
+ *   - Conditions only the device can see (an expert id outside [0, E), an
+ *     expert offset that is misaligned or runs past weight_pack_bytes, a
+ *     pipeline wait that timed out) set bits of a device status word in the
+ *     workspace (moe_read_status); the offending rows or experts are skipped,
+ *     never accessed out of bounds.
+ *   - The stream is a cudaStream_t (0 = legacy default stream).
+ */
+#ifndef MOE_PREFILL_H
+#define MOE_PREFILL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* == cudaStream_t */
+
+/* Weight formats.
+ * MOE_FMT_W2  : 64 values per 18-byte block: fp16 scale d (little endian,
+ *               bytes 0-1), then 16 bytes of 2-bit codes c; code j sits in
+ *               byte 2 + j/4 at bit 2*(j%4).  Value = d*(c-2).
+ * MOE_FMT_W4NL: 32 values per 18-byte block: fp16 d, then 16 bytes of 4-bit
+ *               indices; index j sits in byte 2 + j/2, low nibble for even j.
+ *               Value = d*T[idx], T = {-127,-104,-83,-65,-49,-35,-22,-10,1,
+ *               13,25,38,53,69,89,113}.
+ * A weight matrix [rows x K] is row-major, each row its blocks back to back. */
+enum { MOE_FMT_W2 = 1, MOE_FMT_W4NL = 2 };
+
+/* Gate/up row order: gate rows 0..n_ff-1, then up rows n_ff..2*n_ff-1. */
+enum { MOE_GU_SPLIT = 0 };
+
+enum {
+  MOE_OK = 0,
+  MOE_ERR_NULL = -1,        /* a required pointer is NULL                  */
+  MOE_ERR_SHAPE = -2,       /* T, d, n_ff, E or k out of the supported set */
+  MOE_ERR_FORMAT = -3,      /* unknown weight format or gate/up layout     */
+  MOE_ERR_ALIGN = -4,       /* a pointer is not aligned as documented      */
+  MOE_ERR_WORKSPACE = -5,   /* workspace smaller than moe_prefill_workspace_bytes */
+  MOE_ERR_DEVICE = -6,      /* no sm_103 device is current                 */
+  MOE_ERR_LAUNCH = -7,      /* a CUDA call failed while enqueueing         */
+  MOE_ERR_DEVICE_STATUS = -8 /* moe_read_status found device-side errors   */
+};
+
+/* Device status bits (moe_read_status). */
+enum {
+  MOE_STATUS_BAD_EXPERT_ID = 1,   /* a topk id outside [0, E): row dropped  */
+  MOE_STATUS_BAD_OFFSET = 2,      /* an expert offset misaligned or past the pack: expert skipped */
+  MOE_STATUS_PIPE_TIMEOUT = 4,    /* a bounded pipeline wait gave up        */
+  MOE_STATUS_BAD_ROUTING = 8      /* a stage found routing data that moe_route
+                                     did not write (stage API misuse): skipped */
+};
+
+/* Supported shapes: T >= 0; d and n_ff multiples of 64, 64 <= d <= 8192,
+ * 64 <= n_ff <= 4096; 1 <= E <= 1024; 1 <= k <= E; T*k < 2^24. */
+typedef struct MoeLayerDesc {
+  int32_t T;        /* tokens                                        */
+  int32_t d;        /* hidden size (gate/up K, down output rows)      */
+  int32_t n_ff;     /* expert width (down K)                          */
+  int32_t E;        /* experts                                        */
+  int32_t k;        /* experts per token (top-k)                      */
+  int32_t gu_fmt;   /* MOE_FMT_* of the gate/up matrices              */
+  int32_t down_fmt; /* MOE_FMT_* of the down matrices                 */
+  int32_t gu_layout;/* MOE_GU_SPLIT                                   */
+  uint32_t flags;   /* must be 0                                      */
+  int32_t reserved; /* must be 0                                      */
+  int64_t weight_pack_bytes; /* size of weight_pack; expert matrices must lie inside */
+} MoeLayerDesc;
+
+/* Device pointers into a workspace, as laid out by this library.  Every
+ * region is 256-byte aligned.  R = T*k (rows of entries with a valid id come
+ * first; offsets[E] is the number of valid rows).
+ *   counts  int32 [E]        rows per expert
+ *   offsets int32 [E+1]      exclusive prefix sum of counts
+ *   order   int32 [E]        expert ids by count, largest first, ties by id
+ *   row_src int32 [R]        routed row -> flat entry t*k+r
+ *   dst_of  int32 [R]        flat entry -> routed row (-1 if its id is bad)
+ *   xq      fp16  [T*d]      q8 values of x as exact fp16 integers
+ *   dx      fp32  [T*d/32]   q8 scales of x
+ *   gu      fp32  [R*2*n_ff] gate/up rows (gate half, then up half)
+ *   hq      fp16  [R*n_ff]   q8 values of H as exact fp16 integers
+ *   dh      fp32  [R*n_ff/32] q8 scales of H
+ *   dm      fp32  [R*d]      down rows
+ *   status  int32 [1]        MOE_STATUS_* bits */
+typedef struct MoeWorkspaceView {
+  int32_t *counts, *offsets, *order, *row_src, *dst_of;
+  uint16_t *xq;
+  float *dx, *gu;
+  uint16_t *hq;
+  float *dh, *dm;
+  int32_t *status;
+} MoeWorkspaceView;
+
+/* Bytes of device workspace the layer and the stage entry points need for
+ * `desc` (0 if desc is invalid).  Host only. */
+size_t moe_prefill_workspace_bytes(const MoeLayerDesc *desc);
+
+/* Fill `view` with the device addresses of the workspace regions.  Host
+ * only; returns MOE_OK or an error code. */
+int moe_workspace_view(const MoeLayerDesc *desc, void *workspace,
+                       size_t workspace_bytes, MoeWorkspaceView *view);
+
+/* The whole layer: route -> q8 -> gate/up -> swiglu_quant -> down -> combine.
+ *   x              device fp32 [T x d], row-major
+ *   topk_ids       device int32 [T x k], expert of each (token, rank)
+ *   topk_w         device fp32 [T x k], combine weight of each (token, rank)
+ *   weight_pack    device bytes [weight_pack_bytes], 16-byte aligned
+ *   expert_offsets device int64 [E x 2]: byte offsets in weight_pack of expert
+ *                  e's gate/up matrix [2*n_ff x d] and down matrix [d x n_ff];
+ *                  each must be a multiple of 16 ("a per-layer offset table,
+ *                  + the down offset", Strata #3752 commit "moe_ws kernels")
+ *   out            device fp32 [T x d]
+ *   workspace      device, 256-byte aligned, >= moe_prefill_workspace_bytes
+ * Returns MOE_OK once everything is enqueued on `stream`. */
+int moe_prefill_layer(const MoeLayerDesc *desc, const float *x,
+                      const int32_t *topk_ids, const float *topk_w,
+                      const uint8_t *weight_pack, const int64_t *expert_offsets,
+                      float *out, void *workspace, size_t workspace_bytes,
+                      moe_stream_t stream);
+
+/* The same layer with x, topk_ids, topk_w and out in HOST memory (pinned
+ * memory makes the copies asynchronous; pageable memory works but the copies
+ * then synchronise).  The weights, offsets and workspace stay on the device.
+ * The host inputs are copied into `io`, a caller-owned device staging buffer
+ * of moe_host_io_bytes(desc) bytes (256-byte aligned), with one
+ * cudaMemcpyAsync per array; out is copied back the same way.  The call
+ * returns after enqueueing: the caller synchronises `stream` before reading
+ * out or reusing the host inputs. */
+size_t moe_host_io_bytes(const MoeLayerDesc *desc);
+int moe_prefill_layer_host(const MoeLayerDesc *desc, const float *h_x,
+                           const int32_t *h_topk_ids, const float *h_topk_w,
+                           const uint8_t *weight_pack,
+                           const int64_t *expert_offsets, float *h_out,
+                           void *io, size_t io_bytes, void *workspace,
+                           size_t workspace_bytes, moe_stream_t stream);
+
+/* Stage entry points (tests and profiling).  Each runs one step of the
+ * layer, reading and writing the workspace regions of MoeWorkspaceView, in
+ * the order route, quant_q8, gate_up, swiglu_quant, down, combine (a stage
+ * run on a workspace that moe_route has not filled reads garbage routing data;
+ * it bounds-checks it, skips what is out of range and sets
+ * MOE_STATUS_BAD_ROUTING, never reading or writing outside the buffers).  A later
+ * stage may be re-run on workspace contents written by the caller (for
+ * example the down product alone on a reference Hq). */
+int moe_route(const MoeLayerDesc *desc, const int32_t *topk_ids,
+              void *workspace, size_t workspace_bytes, moe_stream_t stream);
+int moe_quant_q8(const MoeLayerDesc *desc, const float *x, void *workspace,
+                 size_t workspace_bytes, moe_stream_t stream);
+int moe_gate_up(const MoeLayerDesc *desc, const uint8_t *weight_pack,
+                const int64_t *expert_offsets, void *workspace,
+                size_t workspace_bytes, moe_stream_t stream);
+int moe_swiglu_quant(const MoeLayerDesc *desc, void *workspace,
+                     size_t workspace_bytes, moe_stream_t stream);
+int moe_down(const MoeLayerDesc *desc, const uint8_t *weight_pack,
+             const int64_t *expert_offsets, void *workspace,
+             size_t workspace_bytes, moe_stream_t stream);
+int moe_combine(const MoeLayerDesc *desc, const float *topk_w, float *out,
+                void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* Synchronise `stream`, copy the device status word of the workspace to
+ * *status, and clear it on the device.  Returns MOE_OK, or
+ * MOE_ERR_DEVICE_STATUS when any bit was set. */
+int moe_read_status(const MoeLayerDesc *desc, void *workspace,
+                    size_t workspace_bytes, int32_t *status,
+                    moe_stream_t stream);
+
+/* MOE_OK when the current CUDA device is an sm_103 part, else MOE_ERR_DEVICE. */
+int moe_check_device(void);
+
+/* Human-readable text of a MOE_* code (static storage). */
+const char *moe_status_string(int code);
+
+/* Kernels this library has launched in this process (all threads). */
+uint64_t moe_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_PREFILL_H */

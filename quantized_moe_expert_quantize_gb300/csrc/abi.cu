@@ -1,0 +1,370 @@
+// C ABI of libmoeprefill.so: argument validation, workspace layout and the
+// order of the stages.  See include/moe_prefill.h for the contract.
+#include <atomic>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace moe {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 1;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+  size_t status, counts, offsets, order, row_src, dst_of, hist, xq, dx, gu, hq, dh, dm;
+  size_t total;
+};
+
+inline int64_t rows_max(const MoeLayerDesc& d) { return (int64_t)d.T * d.k; }
+
+Layout layout(const MoeLayerDesc& d) {
+  Layout L{};
+  size_t p = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = p;
+    p = align_up(p + bytes);
+    return o;
+  };
+  const int64_t R = rows_max(d);
+  const int nchunks = route_chunks(R);
+  L.status = take(kAlign);
+  L.counts = take(sizeof(int32_t) * d.E);
+  L.offsets = take(sizeof(int32_t) * (d.E + 1));
+  L.order = take(sizeof(int32_t) * d.E);
+  L.row_src = take(sizeof(int32_t) * R);
+  L.dst_of = take(sizeof(int32_t) * R);
+  L.hist = take(sizeof(int32_t) * (size_t)nchunks * d.E);
+  L.xq = take(sizeof(uint16_t) * (size_t)d.T * d.d);
+  L.dx = take(sizeof(float) * (size_t)d.T * (d.d / kQBlock));
+  L.gu = take(sizeof(float) * (size_t)R * 2 * d.n_ff);
+  L.hq = take(sizeof(uint16_t) * (size_t)R * d.n_ff);
+  L.dh = take(sizeof(float) * (size_t)R * (d.n_ff / kQBlock));
+  L.dm = take(sizeof(float) * (size_t)R * d.d);
+  L.total = p;
+  return L;
+}
+
+int validate_desc(const MoeLayerDesc* d) {
+  if (!d) return MOE_ERR_NULL;
+  if (d->T < 0 || d->d < 64 || d->d > 8192 || d->d % 64 != 0 || d->n_ff < 64 ||
+      d->n_ff > 4096 || d->n_ff % 64 != 0 || d->E < 1 || d->E > 1024 || d->k < 1 ||
+      d->k > d->E)
+    return MOE_ERR_SHAPE;
+  if ((int64_t)d->T * d->k >= ((int64_t)1 << 24)) return MOE_ERR_SHAPE;
+  if ((d->gu_fmt != MOE_FMT_W2 && d->gu_fmt != MOE_FMT_W4NL) ||
+      (d->down_fmt != MOE_FMT_W2 && d->down_fmt != MOE_FMT_W4NL) ||
+      d->gu_layout != MOE_GU_SPLIT || d->flags != 0 || d->reserved != 0)
+    return MOE_ERR_FORMAT;
+  if (d->weight_pack_bytes < 0) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int check_device() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_DEVICE;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MOE_ERR_DEVICE;
+  return (major == 10 && minor == 3) ? MOE_OK : MOE_ERR_DEVICE;
+}
+
+struct Ctx {
+  MoeLayerDesc d;
+  Layout L;
+  uint8_t* ws;
+  MoeWorkspaceView v;
+};
+
+int open_ctx(const MoeLayerDesc* desc, void* workspace, size_t bytes, Ctx& c) {
+  int rc = validate_desc(desc);
+  if (rc) return rc;
+  if (!workspace) return MOE_ERR_NULL;
+  if (!aligned(workspace, kAlign)) return MOE_ERR_ALIGN;
+  c.d = *desc;
+  c.L = layout(c.d);
+  if (bytes < c.L.total) return MOE_ERR_WORKSPACE;
+  c.ws = static_cast<uint8_t*>(workspace);
+  auto at = [&](size_t off) { return (void*)(c.ws + off); };
+  c.v.status = (int32_t*)at(c.L.status);
+  c.v.counts = (int32_t*)at(c.L.counts);
+  c.v.offsets = (int32_t*)at(c.L.offsets);
+  c.v.order = (int32_t*)at(c.L.order);
+  c.v.row_src = (int32_t*)at(c.L.row_src);
+  c.v.dst_of = (int32_t*)at(c.L.dst_of);
+  c.v.xq = (uint16_t*)at(c.L.xq);
+  c.v.dx = (float*)at(c.L.dx);
+  c.v.gu = (float*)at(c.L.gu);
+  c.v.hq = (uint16_t*)at(c.L.hq);
+  c.v.dh = (float*)at(c.L.dh);
+  c.v.dm = (float*)at(c.L.dm);
+  return MOE_OK;
+}
+
+inline int launch_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH; }
+
+// The status word starts every layer (and every moe_route) at zero.
+int run_route(Ctx& c, const int32_t* ids, cudaStream_t st) {
+  if (cudaMemsetAsync(c.v.status, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_LAUNCH;
+  return launch_rc(launch_route(ids, rows_max(c.d), c.d.E, (int32_t*)(c.ws + c.L.hist),
+                                c.v.counts, c.v.offsets, c.v.order, c.v.row_src, c.v.dst_of,
+                                c.v.status, st));
+}
+
+int run_quant(Ctx& c, const float* x, cudaStream_t st) {
+  return launch_rc(launch_quant_q8(x, c.d.T, c.d.d, (__half*)c.v.xq, c.v.dx, st));
+}
+
+int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaStream_t st) {
+  GemmArgs a{};
+  a.pack = pack;
+  a.eoff = eoff;
+  a.which = which;
+  a.fmt = which == 0 ? c.d.gu_fmt : c.d.down_fmt;
+  a.pack_bytes = c.d.weight_pack_bytes;
+  a.counts = c.v.counts;
+  a.offsets = c.v.offsets;
+  a.order = c.v.order;
+  a.E = c.d.E;
+  a.k_top = c.d.k;
+  a.status = c.v.status;
+  a.rows_max = rows_max(c.d);
+  if (which == 0) {
+    a.act = (const __half*)c.v.xq;
+    a.act_d = c.v.dx;
+    a.row_src = c.v.row_src;
+    a.K = c.d.d;
+    a.N_out = 2 * c.d.n_ff;
+    a.out = c.v.gu;
+    a.act_rows = c.d.T;
+  } else {
+    a.act = (const __half*)c.v.hq;
+    a.act_d = c.v.dh;
+    a.row_src = nullptr;
+    a.K = c.d.n_ff;
+    a.N_out = c.d.d;
+    a.out = c.v.dm;
+    a.act_rows = rows_max(c.d);
+  }
+  return launch_rc(launch_gemm(a, st));
+}
+
+int run_swiglu(Ctx& c, cudaStream_t st) {
+  return launch_rc(launch_swiglu_quant(c.v.gu, c.v.offsets + c.d.E, rows_max(c.d), c.d.n_ff,
+                                       (__half*)c.v.hq, c.v.dh, st));
+}
+
+int run_combine(Ctx& c, const float* w, float* out, cudaStream_t st) {
+  return launch_rc(launch_combine(w, c.v.dst_of, c.v.dm, c.d.T, c.d.k, c.d.d, out, st));
+}
+
+int check_weights(const MoeLayerDesc* d, const uint8_t* pack, const int64_t* eoff) {
+  if (!pack || !eoff) return MOE_ERR_NULL;
+  if (!aligned(pack, 16) || !aligned(eoff, 8)) return MOE_ERR_ALIGN;
+  (void)d;
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_prefill_workspace_bytes(const MoeLayerDesc* desc) {
+  if (validate_desc(desc)) return 0;
+  return layout(*desc).total;
+}
+
+int moe_workspace_view(const MoeLayerDesc* desc, void* workspace, size_t bytes,
+                       MoeWorkspaceView* view) {
+  if (!view) return MOE_ERR_NULL;
+  Ctx c;
+  const int rc = open_ctx(desc, workspace, bytes, c);
+  if (rc) return rc;
+  *view = c.v;
+  return MOE_OK;
+}
+
+int moe_check_device(void) { return check_device(); }
+
+int moe_route(const MoeLayerDesc* desc, const int32_t* topk_ids, void* ws, size_t bytes,
+              moe_stream_t stream) {
+  Ctx c;
+  int rc = open_ctx(desc, ws, bytes, c);
+  if (rc) return rc;
+  if (!topk_ids && rows_max(c.d) > 0) return MOE_ERR_NULL;
+  if ((rc = check_device())) return rc;
+  return run_route(c, topk_ids, (cudaStream_t)stream);
+}
+
+int moe_quant_q8(const MoeLayerDesc* desc, const float* x, void* ws, size_t bytes,
+                 moe_stream_t stream) {
+  Ctx c;
+  int rc = open_ctx(desc, ws, bytes, c);
+  if (rc) return rc;
+  if (!x && c.d.T > 0) return MOE_ERR_NULL;
+  if (!aligned(x, 16)) return MOE_ERR_ALIGN;
+  if ((rc = check_device())) return rc;
+  return run_quant(c, x, (cudaStream_t)stream);
+}
+
+int moe_gate_up(const MoeLayerDesc* desc, const uint8_t* pack, const int64_t* eoff, void* ws,
+                size_t bytes, moe_stream_t stream) {
+  Ctx c;
+  int rc = open_ctx(desc, ws, bytes, c);
+  if (rc) return rc;
+  if ((rc = check_weights(desc, pack, eoff))) return rc;
+  if ((rc = check_device())) return rc;
+  return run_gemm(c, 0, pack, eoff, (cudaStream_t)stream);
+}
+
+int moe_swiglu_quant(const MoeLayerDesc* desc, void* ws, size_t bytes, moe_stream_t stream) {
+  Ctx c;
+  int rc = open_ctx(desc, ws, bytes, c);
+  if (rc) return rc;
+  if ((rc = check_device())) return rc;
+  return run_swiglu(c, (cudaStream_t)stream);
+}
+
+int moe_down(const MoeLayerDesc* desc, const uint8_t* pack, const int64_t* eoff, void* ws,
+             size_t bytes, moe_stream_t stream) {
+  Ctx c;
+  int rc = open_ctx(desc, ws, bytes, c);
+  if (rc) return rc;
+  if ((rc = check_weights(desc, pack, eoff))) return rc;
+  if ((rc = check_device())) return rc;
+  return run_gemm(c, 1, pack, eoff, (cudaStream_t)stream);
+}
+
+int moe_combine(const MoeLayerDesc* desc, const float* topk_w, float* out, void* ws, size_t bytes,
+                moe_stream_t stream) {
+  Ctx c;
+  int rc = open_ctx(desc, ws, bytes, c);
+  if (rc) return rc;
+  if ((!topk_w || !out) && c.d.T > 0) return MOE_ERR_NULL;
+  if (!aligned(out, 16)) return MOE_ERR_ALIGN;
+  if ((rc = check_device())) return rc;
+  return run_combine(c, topk_w, out, (cudaStream_t)stream);
+}
+
+int moe_prefill_layer(const MoeLayerDesc* desc, const float* x, const int32_t* topk_ids,
+                      const float* topk_w, const uint8_t* weight_pack,
+                      const int64_t* expert_offsets, float* out, void* ws, size_t bytes,
+                      moe_stream_t stream) {
+  Ctx c;
+  int rc = open_ctx(desc, ws, bytes, c);
+  if (rc) return rc;
+  if (c.d.T > 0 && (!x || !topk_ids || !topk_w || !out)) return MOE_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(topk_ids, 4) || !aligned(topk_w, 4))
+    return MOE_ERR_ALIGN;
+  if ((rc = check_weights(desc, weight_pack, expert_offsets))) return rc;
+  if ((rc = check_device())) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((rc = run_route(c, topk_ids, st))) return rc;
+  if ((rc = run_quant(c, x, st))) return rc;
+  if ((rc = run_gemm(c, 0, weight_pack, expert_offsets, st))) return rc;
+  if ((rc = run_swiglu(c, st))) return rc;
+  if ((rc = run_gemm(c, 1, weight_pack, expert_offsets, st))) return rc;
+  return run_combine(c, topk_w, out, st);
+}
+
+size_t moe_host_io_bytes(const MoeLayerDesc* desc) {
+  if (validate_desc(desc)) return 0;
+  const size_t T = (size_t)desc->T;
+  return align_up(sizeof(float) * T * desc->d) + align_up(sizeof(int32_t) * T * desc->k) +
+         align_up(sizeof(float) * T * desc->k) + align_up(sizeof(float) * T * desc->d);
+}
+
+int moe_prefill_layer_host(const MoeLayerDesc* desc, const float* h_x, const int32_t* h_ids,
+                           const float* h_w, const uint8_t* weight_pack,
+                           const int64_t* expert_offsets, float* h_out, void* io,
+                           size_t io_bytes, void* ws, size_t bytes, moe_stream_t stream) {
+  Ctx c;
+  int rc = open_ctx(desc, ws, bytes, c);
+  if (rc) return rc;
+  if (c.d.T > 0 && (!h_x || !h_ids || !h_w || !h_out)) return MOE_ERR_NULL;
+  if (!io) return MOE_ERR_NULL;
+  if (!aligned(io, kAlign)) return MOE_ERR_ALIGN;
+  if (io_bytes < moe_host_io_bytes(desc)) return MOE_ERR_WORKSPACE;
+  if ((rc = check_weights(desc, weight_pack, expert_offsets))) return rc;
+  if ((rc = check_device())) return rc;
+  const size_t T = (size_t)c.d.T;
+  const size_t bx = sizeof(float) * T * c.d.d, bi = sizeof(int32_t) * T * c.d.k,
+               bw = sizeof(float) * T * c.d.k;
+  uint8_t* p = static_cast<uint8_t*>(io);
+  float* d_x = (float*)p;
+  int32_t* d_ids = (int32_t*)(p + align_up(bx));
+  float* d_w = (float*)(p + align_up(bx) + align_up(bi));
+  float* d_out = (float*)(p + align_up(bx) + align_up(bi) + align_up(bw));
+  cudaStream_t st = (cudaStream_t)stream;
+  if (T > 0) {
+    if (cudaMemcpyAsync(d_x, h_x, bx, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(d_ids, h_ids, bi, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(d_w, h_w, bw, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return MOE_ERR_LAUNCH;
+  }
+  if ((rc = run_route(c, d_ids, st))) return rc;
+  if ((rc = run_quant(c, d_x, st))) return rc;
+  if ((rc = run_gemm(c, 0, weight_pack, expert_offsets, st))) return rc;
+  if ((rc = run_swiglu(c, st))) return rc;
+  if ((rc = run_gemm(c, 1, weight_pack, expert_offsets, st))) return rc;
+  if ((rc = run_combine(c, d_w, d_out, st))) return rc;
+  if (T > 0 && cudaMemcpyAsync(h_out, d_out, bx, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_LAUNCH;
+  return MOE_OK;
+}
+
+int moe_read_status(const MoeLayerDesc* desc, void* ws, size_t bytes, int32_t* status,
+                    moe_stream_t stream) {
+  Ctx c;
+  int rc = open_ctx(desc, ws, bytes, c);
+  if (rc) return rc;
+  if (!status) return MOE_ERR_NULL;
+  if ((rc = check_device())) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, c.v.status, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemsetAsync(c.v.status, 0, sizeof(int32_t), st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return MOE_ERR_LAUNCH;
+  *status = v;
+  return v ? MOE_ERR_DEVICE_STATUS : MOE_OK;
+}
+
+const char* moe_status_string(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_NULL: return "a required pointer is NULL";
+    case MOE_ERR_SHAPE: return "unsupported shape";
+    case MOE_ERR_FORMAT: return "unknown weight format, layout or flags";
+    case MOE_ERR_ALIGN: return "misaligned pointer";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_DEVICE: return "no sm_103 device is current";
+    case MOE_ERR_LAUNCH: return "a CUDA call failed while enqueueing";
+    case MOE_ERR_DEVICE_STATUS: return "device-side status bits were set";
+    default: return "unknown status code";
+  }
+}
+
+uint64_t moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

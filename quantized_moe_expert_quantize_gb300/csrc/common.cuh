@@ -1,0 +1,79 @@
+// Shared device/host helpers of the CUDA library (not of the oracle).
+#pragma once
+#include <cstdint>
+#include <cstddef>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "moe_prefill.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------- formats
+constexpr int kBlockBytes = 18;       // W2 and W4NL blocks are 18 bytes
+constexpr int kW2Values = 64;         // values per W2 block
+constexpr int kW4Values = 32;         // values per W4NL block
+constexpr int kQBlock = 32;           // q8 block of activations
+
+__host__ __device__ inline int block_values(int fmt) { return fmt == MOE_FMT_W2 ? kW2Values : kW4Values; }
+__host__ __device__ inline int64_t row_bytes(int fmt, int K) {
+  return (int64_t)(K / block_values(fmt)) * kBlockBytes;
+}
+
+// fp16 bit patterns of the integers -2..1 (W2 codes 0..3 minus 2).
+constexpr uint64_t kW2HalfLut = 0x3C000000BC00C000ull;
+
+// fp16 bit patterns of the W4NL table {-127,-104,-83,-65,-49,-35,-22,-10,
+// 1,13,25,38,53,69,89,113} (exact: every entry has at most 7 significant bits).
+__constant__ const uint16_t c_nl4_half[16] = {
+    0xD7F0, 0xD680, 0xD530, 0xD410, 0xD220, 0xD060, 0xCD80, 0xC900,
+    0x3C00, 0x4A80, 0x4E40, 0x50C0, 0x52A0, 0x5450, 0x5590, 0x5710};
+
+// ------------------------------------------------------------- launch count
+void count_launch(int n = 1);
+
+// -------------------------------------------------------------- route
+constexpr int kRouteChunk = 1024;  // flat entries per warp
+constexpr int kRouteWarps = 8;     // warps per CTA
+inline int route_chunks(int64_t n) { return (int)((n + kRouteChunk - 1) / kRouteChunk); }
+
+cudaError_t launch_route(const int32_t* ids, int64_t n, int E, int32_t* hist,
+                         int32_t* counts, int32_t* offsets, int32_t* order,
+                         int32_t* row_src, int32_t* dst_of, int32_t* status,
+                         cudaStream_t st);
+
+// ---------------------------------------------------- elementwise kernels
+cudaError_t launch_quant_q8(const float* x, int64_t rows, int K, __half* q, float* d,
+                            cudaStream_t st);
+cudaError_t launch_swiglu_quant(const float* gu, const int32_t* nrows_dev, int64_t rows_max,
+                                int n_ff, __half* hq, float* dh, cudaStream_t st);
+cudaError_t launch_combine(const float* topk_w, const int32_t* dst_of, const float* dm,
+                           int64_t T, int k, int d, float* out, cudaStream_t st);
+
+// ------------------------------------------------------------ products
+struct GemmArgs {
+  const uint8_t* pack;       // weight pack
+  const int64_t* eoff;       // [E][2] byte offsets
+  int which;                 // 0 = gate/up, 1 = down
+  int fmt;                   // MOE_FMT_*
+  int64_t pack_bytes;
+  const int32_t* counts;     // [E]
+  const int32_t* offsets;    // [E+1]
+  const int32_t* order;      // [E] largest first
+  int E;
+  const __half* act;         // activation values (exact fp16 integers)
+  const float* act_d;        // activation scales, one per 32 values
+  const int32_t* row_src;    // gather: routed row -> flat entry (token = entry / k_top); null = no gather
+  int k_top;
+  int K;                     // reduction length
+  int N_out;                 // output columns (weight rows)
+  float* out;                // [rows x N_out]
+  int64_t rows_max;          // capacity of the routed-row buffers (T*k)
+  int64_t act_rows;          // rows of act (T for gate/up, T*k for down)
+  int32_t* status;
+};
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st);
+
+int device_sm_count();
+
+}  // namespace moe

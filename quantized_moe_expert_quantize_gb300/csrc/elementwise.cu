@@ -1,0 +1,161 @@
+// Bandwidth-bound steps of the layer:
+//   quant_q8      -- x -> q8 per 32-value block ("Strata #3752", commit
+//                    "swiglu_quant": quantize_mmq_q8_1; layer spec, tiny
+//                    configuration: d = amax/127, q = rint(x/d), d = 0 -> 0);
+//   swiglu_quant  -- H = silu(g)*u and its q8 in one pass, H never stored
+//                    ("Strata #3752", commit "swiglu_quant");
+//   combine       -- out[t] = sum over ranks r = 0..k-1 of w[t,r]*Dm[row]
+//                    (layer spec, tiny configuration).
+//
+// Quantised values are stored as exact fp16 integers (|q| <= 127): that is
+// the operand type of the fp16 tensor-core products, and it carries the same
+// information as the int8 code.
+//
+// Every division is IEEE (__fdiv_rn), rounding to integer is rintf (half to
+// even), and the q8 decisions are taken in fp32 exactly as the method states.
+// This file must not be compiled with fast-math.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+// Quantise 8 consecutive values held by one thread; four consecutive lanes
+// hold one 32-value block.  Returns the block scale.
+__device__ __forceinline__ float q8_group8(const float (&v)[8], uint4& packed) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; i++) amax = fmaxf(amax, fabsf(v[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  const float d = __fdiv_rn(amax, 127.0f);
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    const float q0 = (d == 0.0f) ? 0.0f : rintf(__fdiv_rn(v[2 * i], d));
+    const float q1 = (d == 0.0f) ? 0.0f : rintf(__fdiv_rn(v[2 * i + 1], d));
+    const __half2 h = __floats2half2_rn(q0, q1);  // exact: |q| <= 127
+    w[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  packed = make_uint4(w[0], w[1], w[2], w[3]);
+  return d;
+}
+
+__global__ void __launch_bounds__(256)
+quant_q8_kernel(const float* __restrict__ x, int64_t groups, __half* __restrict__ q,
+                float* __restrict__ d) {
+  const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const bool ok = g < groups;  // groups is a multiple of 4: quads are whole
+  float v[8];
+  if (ok) {
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(x) + 2 * g);
+    const float4 b = __ldcs(reinterpret_cast<const float4*>(x) + 2 * g + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; i++) v[i] = 0.0f;
+  }
+  uint4 packed;
+  const float db = q8_group8(v, packed);
+  if (ok) {
+    reinterpret_cast<uint4*>(q)[g] = packed;
+    if ((g & 3) == 0) d[g >> 2] = db;
+  }
+}
+
+__global__ void __launch_bounds__(256)
+swiglu_quant_kernel(const float* __restrict__ gu, const int32_t* __restrict__ nrows_dev,
+                    int64_t rows_max, int n_ff, __half* __restrict__ hq, float* __restrict__ dh) {
+  const int per_row = n_ff / 8;
+  // rows actually routed, clamped to the buffers (a stale count cannot overrun)
+  const int64_t nrows = min((int64_t)max(*nrows_dev, 0), rows_max);
+  const int64_t groups = nrows * per_row;
+  const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const bool ok = g < groups;
+  float v[8];
+  if (ok) {
+    const int64_t row = g / per_row;
+    const int c = (int)(g - row * per_row);
+    const float4* gp = reinterpret_cast<const float4*>(gu + row * 2 * n_ff + c * 8);
+    const float4* up = reinterpret_cast<const float4*>(gu + row * 2 * n_ff + n_ff + c * 8);
+    const float4 g0 = __ldcs(gp), g1 = __ldcs(gp + 1), u0 = __ldcs(up), u1 = __ldcs(up + 1);
+    const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      // silu(g) * u = (g / (1 + exp(-g))) * u, each step rounded to fp32
+      const float den = __fadd_rn(1.0f, expf(-gv[i]));
+      v[i] = __fmul_rn(__fdiv_rn(gv[i], den), uv[i]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; i++) v[i] = 0.0f;
+  }
+  uint4 packed;
+  const float db = q8_group8(v, packed);
+  if (ok) {
+    reinterpret_cast<uint4*>(hq)[g] = packed;
+    if ((g & 3) == 0) dh[g >> 2] = db;
+  }
+}
+
+__global__ void __launch_bounds__(256)
+combine_kernel(const float* __restrict__ topk_w, const int32_t* __restrict__ dst_of,
+               const float4* __restrict__ dm, int64_t T, int k, int d4,
+               float4* __restrict__ out) {
+  const int64_t rows_max = T * k;
+  const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= T * d4) return;
+  const int64_t t = g / d4;
+  const int c = (int)(g - t * d4);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int r = 0; r < k; r++) {
+    const int32_t pos = dst_of[t * k + r];
+    if (pos < 0 || pos >= rows_max) continue;  // dropped row (bad expert id)
+    const float w = topk_w[t * k + r];
+    const float4 v = __ldcs(dm + (int64_t)pos * d4 + c);
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
+  }
+  out[g] = acc;
+}
+
+inline unsigned blocks_for(int64_t threads, int per_block) {
+  return (unsigned)((threads + per_block - 1) / per_block);
+}
+
+}  // namespace
+
+cudaError_t launch_quant_q8(const float* x, int64_t rows, int K, __half* q, float* d,
+                            cudaStream_t st) {
+  const int64_t groups = rows * (K / 8);
+  if (groups == 0) return cudaSuccess;
+  quant_q8_kernel<<<blocks_for(groups, 256), 256, 0, st>>>(x, groups, q, d);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_quant(const float* gu, const int32_t* nrows_dev, int64_t rows_max,
+                                int n_ff, __half* hq, float* dh, cudaStream_t st) {
+  const int64_t groups = rows_max * (n_ff / 8);
+  if (groups == 0) return cudaSuccess;
+  swiglu_quant_kernel<<<blocks_for(groups, 256), 256, 0, st>>>(gu, nrows_dev, rows_max, n_ff,
+                                                                hq, dh);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* topk_w, const int32_t* dst_of, const float* dm,
+                           int64_t T, int k, int d, float* out, cudaStream_t st) {
+  const int64_t n = T * (d / 4);
+  if (n == 0) return cudaSuccess;
+  combine_kernel<<<blocks_for(n, 256), 256, 0, st>>>(
+      topk_w, dst_of, reinterpret_cast<const float4*>(dm), T, k, d / 4,
+      reinterpret_cast<float4*>(out));
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,155 @@
+// Routing: histogram of the top-k expert ids, exclusive prefix sum, and the
+// stable permutation of the T*k flat rows into expert buckets
+// ("Strata #3752", commits "moe_ws wiring" and "swiglu_quant landed":
+// quantize_scatter, the group bounds uploaded with the layer).
+//
+// Three small kernels, all integer and bit-exact:
+//   1. route_hist    -- one warp per chunk of 1024 flat entries counts the
+//                       chunk's rows per expert (shared-memory histogram);
+//   2. route_scan    -- one CTA turns the [chunk][expert] counts into the
+//                       base row of every (chunk, expert), the expert counts,
+//                       their exclusive prefix sum (group bounds) and the
+//                       largest-first expert order used by the product
+//                       kernels' schedulers;
+//   3. route_scatter -- each warp walks its chunk again, 32 entries at a
+//                       time; __match_any_sync groups lanes of equal expert,
+//                       a lane's rank among them keeps flat order, so rows of
+//                       a bucket come out in increasing flat index t*k + r.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+__global__ void __launch_bounds__(kRouteWarps * 32)
+route_hist_kernel(const int32_t* __restrict__ ids, int64_t n, int E, int nchunks,
+                  int32_t* __restrict__ hist, int32_t* __restrict__ status) {
+  extern __shared__ int32_t sh[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x * kRouteWarps + warp;
+  int32_t* h = sh + warp * E;
+  if (chunk >= nchunks) return;  // whole warp; no CTA barrier below
+  for (int e = lane; e < E; e += 32) h[e] = 0;
+  __syncwarp();
+  const int64_t beg = (int64_t)chunk * kRouteChunk;
+  const int64_t end = min(n, beg + kRouteChunk);
+  bool bad = false;
+  for (int64_t i = beg + lane; i < end; i += 32) {
+    const int e = ids[i];
+    if ((unsigned)e < (unsigned)E)
+      atomicAdd(&h[e], 1);
+    else
+      bad = true;
+  }
+  if (bad) atomicOr(status, MOE_STATUS_BAD_EXPERT_ID);
+  __syncwarp();
+  for (int e = lane; e < E; e += 32) hist[(int64_t)chunk * E + e] = h[e];
+}
+
+// One CTA of 1024 threads; thread e owns expert e (E <= 1024).
+__global__ void __launch_bounds__(1024)
+route_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E,
+                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                  int32_t* __restrict__ order) {
+  __shared__ int32_t s_cnt[1024];
+  __shared__ int32_t s_warp[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int run = 0;
+  if (tid < E) {
+    for (int c = 0; c < nchunks; c++) {
+      const int64_t idx = (int64_t)c * E + tid;
+      const int v = hist[idx];
+      hist[idx] = run;  // rows of expert tid in chunks before c
+      run += v;
+    }
+    counts[tid] = run;
+  }
+  s_cnt[tid] = run;
+  // exclusive prefix sum of the counts over the CTA
+  int incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = s_warp[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    s_warp[lane] = wi - w;
+  }
+  __syncthreads();
+  const int excl = s_warp[warp] + incl - run;
+  if (tid < E) {
+    offsets[tid] = excl;
+    if (tid == E - 1) offsets[E] = excl + run;
+    for (int c = 0; c < nchunks; c++) hist[(int64_t)c * E + tid] += excl;
+    // rank by (count descending, id ascending)
+    int r = 0;
+    for (int e2 = 0; e2 < E; e2++) {
+      const int c2 = s_cnt[e2];
+      r += (c2 > run) || (c2 == run && e2 < tid);
+    }
+    order[r] = tid;
+  }
+}
+
+__global__ void __launch_bounds__(kRouteWarps * 32)
+route_scatter_kernel(const int32_t* __restrict__ ids, int64_t n, int E, int nchunks,
+                     const int32_t* __restrict__ hist, int32_t* __restrict__ row_src,
+                     int32_t* __restrict__ dst_of) {
+  extern __shared__ int32_t sh[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x * kRouteWarps + warp;
+  int32_t* h = sh + warp * E;
+  if (chunk >= nchunks) return;
+  for (int e = lane; e < E; e += 32) h[e] = hist[(int64_t)chunk * E + e];
+  __syncwarp();
+  const unsigned lt = (1u << lane) - 1u;
+  const int64_t beg = (int64_t)chunk * kRouteChunk;
+  const int64_t end = min(n, beg + kRouteChunk);
+  for (int64_t base = beg; base < end; base += 32) {
+    const int64_t i = base + lane;
+    const bool act = i < end;
+    const int e = act ? ids[i] : -1;
+    const bool valid = act && (unsigned)e < (unsigned)E;
+    const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+    const int rank = __popc(peers & lt);
+    const int pos = valid ? h[e] + rank : -1;
+    __syncwarp();
+    if (valid && rank == 0) h[e] += __popc(peers);
+    __syncwarp();
+    if (valid) row_src[pos] = (int32_t)i;
+    if (act) dst_of[i] = pos;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route(const int32_t* ids, int64_t n, int E, int32_t* hist,
+                         int32_t* counts, int32_t* offsets, int32_t* order,
+                         int32_t* row_src, int32_t* dst_of, int32_t* status,
+                         cudaStream_t st) {
+  const int nchunks = route_chunks(n);
+  const int grid = (nchunks + kRouteWarps - 1) / kRouteWarps;
+  const size_t smem = sizeof(int32_t) * kRouteWarps * E;
+  if (grid > 0) {
+    route_hist_kernel<<<grid, kRouteWarps * 32, smem, st>>>(ids, n, E, nchunks, hist, status);
+    count_launch();
+  }
+  route_scan_kernel<<<1, 1024, 0, st>>>(hist, nchunks, E, counts, offsets, order);
+  count_launch();
+  if (grid > 0) {
+    route_scatter_kernel<<<grid, kRouteWarps * 32, smem, st>>>(ids, n, E, nchunks, hist,
+                                                                row_src, dst_of);
+    count_launch();
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,172 @@
+"""Helpers for the GPU parity tests: upload a synthetic layer, run the library
+through its C ABI (Python binding), and compare with the CPU oracle.
+
+Tolerances (the layer spec's parity bar):
+  routing permutation, q8 of x          bit-exact
+  GU, Dm                                rel RMS <= 1e-5 vs the oracle
+  Hq                                    <= 1e-4 of values differ, each by +-1
+  out                                   rel RMS <= 1e-4
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+TOL_GU = 1e-5
+TOL_DM = 1e-5
+TOL_HQ_FRAC = 1e-4
+TOL_OUT = 1e-4
+
+
+def require_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import quantized_moe_expert_quantize_gb300 as M
+    from quantized_moe_expert_quantize_gb300 import build as B
+    B.build()
+    assert M.moe_check_device() == M.MOE_OK, "current device is not an sm_103 part"
+    return M
+
+
+def rel_rms(a, b) -> float:
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    den = np.sqrt((b ** 2).mean()) if b.size else 0.0
+    if den == 0.0:
+        return 0.0 if np.all(a == b) else float("inf")
+    return float(np.sqrt(((a - b) ** 2).mean()) / den)
+
+
+class DeviceLayer:
+    """A synth.Layer resident on the GPU plus a workspace and views."""
+
+    def __init__(self, M, L: synth.Layer):
+        self.M = M
+        self.L = L
+        s = L.shape
+        self.desc = M.make_desc(s.T, s.d, s.n_ff, s.E, s.k, s.gu_fmt, s.down_fmt,
+                                L.weight_pack.size)
+        dev = "cuda"
+        self.x = torch.from_numpy(L.x).to(dev)
+        self.ids = torch.from_numpy(L.topk_ids).to(dev)
+        self.w = torch.from_numpy(L.topk_w).to(dev)
+        self.pack = torch.from_numpy(L.weight_pack).to(dev)
+        self.eoff = torch.from_numpy(L.expert_offsets).to(dev)
+        self.out = torch.full((max(s.T, 1), s.d), float("nan"), device=dev)[: s.T]
+        self.ws = M.alloc_workspace(self.desc)
+        self.ws.fill_(0xFF)  # poison: nothing may rely on zeroed workspace
+        self.v = M.workspace_view(self.desc, self.ws)
+
+    def run_layer(self):
+        self.M.moe_prefill_layer(self.desc, self.x, self.ids, self.w, self.pack, self.eoff,
+                                 self.out, self.ws)
+        torch.cuda.synchronize()
+
+    def run_stages(self):
+        M = self.M
+        M.moe_route(self.desc, self.ids, self.ws)
+        M.moe_quant_q8(self.desc, self.x, self.ws)
+        M.moe_gate_up(self.desc, self.pack, self.eoff, self.ws)
+        M.moe_swiglu_quant(self.desc, self.ws)
+        M.moe_down(self.desc, self.pack, self.eoff, self.ws)
+        M.moe_combine(self.desc, self.w, self.out, self.ws)
+        torch.cuda.synchronize()
+
+    def status(self) -> int:
+        return self.M.moe_read_status(self.desc, self.ws)
+
+    def get(self, name, rows=None) -> np.ndarray:
+        t = self.v[name]
+        if rows is not None:
+            t = t[:rows]
+        a = t.cpu().numpy()
+        return a
+
+
+def check_route(dl: DeviceLayer, o: dict):
+    s = dl.L.shape
+    R = int(o["offsets"][-1])
+    assert np.array_equal(dl.get("counts"), o["counts"])
+    assert np.array_equal(dl.get("offsets"), o["offsets"])
+    assert np.array_equal(dl.get("row_src", R), o["row_src"])
+    assert np.array_equal(dl.get("dst_of", s.T * s.k), o["dst_of"])
+    order = dl.get("order")
+    # largest first, ties by id: the unique order
+    want = np.lexsort((np.arange(s.E), -o["counts"]))
+    assert np.array_equal(order, want)
+
+
+def check_q8_x(dl: DeviceLayer, o: dict):
+    xq = dl.get("xq").astype(np.float32)
+    assert np.array_equal(xq, o["xq"].astype(np.float32))
+    assert np.array_equal(dl.get("dx"), o["dx"])
+
+
+def hq_compare(hq_gpu: np.ndarray, hq_ref: np.ndarray):
+    """Fraction of differing q8 values and the largest difference."""
+    a = hq_gpu.astype(np.int32)
+    b = hq_ref.astype(np.int32)
+    diff = np.abs(a - b)
+    n = int(np.count_nonzero(diff))
+    return n / max(diff.size, 1), int(diff.max()) if diff.size else 0, n
+
+
+def check_full(dl: DeviceLayer, o: dict, report: dict | None = None):
+    """Every stage of a full run against a full oracle run."""
+    check_route(dl, o)
+    check_q8_x(dl, o)
+    R = int(o["offsets"][-1])
+    gu = dl.get("gu", R)
+    r_gu = rel_rms(gu, o["gu"])
+    assert r_gu <= TOL_GU, r_gu
+    hq = dl.get("hq", R)
+    frac, mx, n = hq_compare(hq, o["hq"])
+    assert frac <= TOL_HQ_FRAC and mx <= 1, (frac, mx, n)
+    dh = dl.get("dh", R)
+    dm = dl.get("dm", R)
+    r_dm = rel_rms(dm, o["dm"])
+    assert r_dm <= TOL_DM, r_dm
+    r_out = rel_rms(dl.out.cpu().numpy(), o["out"])
+    assert r_out <= TOL_OUT, r_out
+    if report is not None:
+        report.update(gu_rel_rms=r_gu, gu_exact=bool(np.array_equal(gu, o["gu"])),
+                      hq_diff=n, dh_exact=bool(np.array_equal(dh, o["dh"])), dm_rel_rms=r_dm,
+                      out_rel_rms=r_out)
+    return dict(gu=r_gu, hq=n, dm=r_dm, out=r_out)
+
+
+def oracle_rows(L: synth.Layer, o_route: dict, xq, dx, rows: np.ndarray):
+    """Oracle GU, Hq, dh and Dm of the routed rows ``rows`` (one at a time)."""
+    s = L.shape
+    src = o_route["row_src"][rows]
+    tok = src // s.k
+    exp = L.topk_ids.reshape(-1)[src]
+    gu = np.zeros((len(rows), 2 * s.n_ff), np.float32)
+    dm = np.zeros((len(rows), s.d), np.float32)
+    for i in range(len(rows)):
+        e = int(exp[i])
+        gu[i] = oracle.expert_rows(s.gu_fmt, s.d, 2 * s.n_ff,
+                                   L.weight_pack[L.expert_offsets[e, 0]:],
+                                   xq[tok[i]][None], dx[tok[i]][None])[0]
+    hq, dh = oracle.swiglu_quant(gu, s.n_ff)
+    for i in range(len(rows)):
+        e = int(exp[i])
+        dm[i] = oracle.expert_rows(s.down_fmt, s.n_ff, s.d,
+                                   L.weight_pack[L.expert_offsets[e, 1]:],
+                                   hq[i][None], dh[i][None])[0]
+    return gu, hq, dh, dm, exp
+
+
+def oracle_down_rows(L: synth.Layer, exp, hq, dh):
+    s = L.shape
+    dm = np.zeros((len(exp), s.d), np.float32)
+    for i in range(len(exp)):
+        e = int(exp[i])
+        dm[i] = oracle.expert_rows(s.down_fmt, s.n_ff, s.d,
+                                   L.weight_pack[L.expert_offsets[e, 1]:],
+                                   hq[i][None], dh[i][None])[0]
+    return dm

@@ -1,0 +1,101 @@
+"""The C ABI on the host, no GPU: the library loads, exports every entry
+point include/moe_prefill.h declares, sizes its workspace, and rejects bad
+arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import quantized_moe_expert_quantize_gb300 as M
+from quantized_moe_expert_quantize_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return M.lib()
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w \*]*?\b(moe_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_binding_exports():
+    assert set(declared_functions()) == set(M.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_workspace_bytes_layout(lib):
+    d = M.make_desc(16384, 2560, 640, 512, 10)
+    n = M.workspace_bytes(d)
+    R = 16384 * 10
+    minimum = R * (2 * 640 * 4 + 640 * 2 + 640 // 32 * 4 + 2560 * 4 + 8) + 16384 * 2560 * 2
+    assert minimum <= n <= minimum + 64 * 2**20
+    assert n % 256 == 0
+    assert M.host_io_bytes(d) >= 2 * 16384 * 2560 * 4
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("d", 100, M.MOE_ERR_SHAPE), ("d", 32, M.MOE_ERR_SHAPE), ("n_ff", 96, M.MOE_ERR_SHAPE),
+    ("E", 0, M.MOE_ERR_SHAPE), ("E", 2048, M.MOE_ERR_SHAPE), ("k", 0, M.MOE_ERR_SHAPE),
+    ("k", 9, M.MOE_ERR_SHAPE), ("T", -1, M.MOE_ERR_SHAPE), ("gu_fmt", 3, M.MOE_ERR_FORMAT),
+    ("down_fmt", 0, M.MOE_ERR_FORMAT), ("gu_layout", 1, M.MOE_ERR_FORMAT),
+    ("flags", 1, M.MOE_ERR_FORMAT)])
+def test_bad_descriptor_rejected(lib, field, value, code):
+    d = M.make_desc(64, 256, 64, 8, 2)
+    setattr(d, field, value)
+    assert lib.moe_prefill_workspace_bytes(ctypes.byref(d)) == 0
+    ws = ctypes.create_string_buffer(1 << 20)
+    rc = lib.moe_prefill_layer(ctypes.byref(d), 16, 16, 16, 16, 16, 16, ctypes.addressof(ws),
+                               1 << 20, None)
+    assert rc == code
+
+
+def _fake(addr):
+    return ctypes.c_void_p(addr)
+
+
+def test_null_misaligned_and_small_workspace(lib):
+    d = M.make_desc(64, 256, 64, 8, 2, weight_pack_bytes=1 << 20)
+    need = lib.moe_prefill_workspace_bytes(ctypes.byref(d))
+    ws = 1 << 40  # never dereferenced: every case below fails validation first
+    dp = ctypes.byref(d)
+    call = lambda *a: lib.moe_prefill_layer(dp, *a)
+    ok = [_fake(0x1000), _fake(0x2000), _fake(0x3000), _fake(0x4000), _fake(0x5000),
+          _fake(0x6000)]
+    # null workspace / inputs
+    assert call(*ok, None, need, None) == M.MOE_ERR_NULL
+    assert call(None, *ok[1:], _fake(ws), need, None) == M.MOE_ERR_NULL
+    assert call(ok[0], ok[1], ok[2], None, ok[4], ok[5], _fake(ws), need, None) == M.MOE_ERR_NULL
+    # workspace too small / misaligned
+    assert call(*ok, _fake(ws), need - 1, None) == M.MOE_ERR_WORKSPACE
+    assert call(*ok, _fake(ws + 16), need, None) == M.MOE_ERR_ALIGN
+    # misaligned x, weight pack
+    assert call(_fake(0x1004), *ok[1:], _fake(ws), need, None) == M.MOE_ERR_ALIGN
+    assert call(ok[0], ok[1], ok[2], _fake(0x4008), ok[4], ok[5], _fake(ws), need,
+                None) == M.MOE_ERR_ALIGN
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device answer")
+def test_no_device_is_reported(lib):
+    assert M.moe_check_device() == M.MOE_ERR_DEVICE
+
+
+def test_status_strings(lib):
+    for code in range(-8, 1):
+        assert M.status_string(code) != "unknown status code"
+    assert M.status_string(-99) == "unknown status code"

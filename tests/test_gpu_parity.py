@@ -1,0 +1,244 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle."""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_harness import (DeviceLayer, TOL_DM, TOL_GU, TOL_HQ_FRAC, TOL_OUT, check_full,
+                         check_q8_x, check_route, hq_compare, oracle_down_rows, oracle_rows,
+                         rel_rms, require_gpu)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def M():
+    return require_gpu()
+
+
+# ------------------------------------------------------------ small layers
+SMALL = {
+    "cfg0_tiny": lambda: synth.config_layer(0),
+    # several tiles per expert with ragged tails, both down formats
+    "mid_w2_w2": lambda: synth.make_layer(synth.LayerShape(300, 512, 192, 16, 4, synth.W2, synth.W2),
+                                          seed=7, routing="topk", bias=True, outliers=True),
+    "mid_w2_w4nl": lambda: synth.make_layer(synth.LayerShape(257, 384, 128, 12, 3, synth.W2, synth.W4NL),
+                                            seed=8, routing="topk", bias=True, outliers=True),
+    "mid_w4nl_w4nl": lambda: synth.make_layer(synth.LayerShape(130, 256, 64, 5, 2, synth.W4NL, synth.W4NL),
+                                              seed=9, routing="topk", bias=False, outliers=True),
+    "flat_w2_w4nl": lambda: synth.make_layer(synth.LayerShape(128, 256, 128, 16, 4, synth.W2, synth.W4NL),
+                                             seed=10, routing="flat", outliers=True),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("mode", ["layer", "stages"])
+def test_small_layer_full_parity(M, name, mode):
+    L = SMALL[name]()
+    o = oracle.layer(L)
+    dl = DeviceLayer(M, L)
+    dl.run_layer() if mode == "layer" else dl.run_stages()
+    assert dl.status() == 0
+    check_full(dl, o)
+
+
+def test_config4_full_parity(M):
+    """T=128 full layer (the weight-bandwidth-bound configuration), every
+    output against the full oracle."""
+    L = synth.config_layer(4)
+    o = oracle.layer(L)
+    dl = DeviceLayer(M, L)
+    dl.run_layer()
+    assert dl.status() == 0
+    check_full(dl, o)
+
+
+def test_down_alone_on_oracle_hq(M):
+    """The down product alone, fed the oracle's Hq (the pages' parity test
+    also ran the down alone on reference H)."""
+    L = SMALL["mid_w2_w4nl"]()
+    o = oracle.layer(L)
+    dl = DeviceLayer(M, L)
+    dl.run_layer()
+    R = int(o["offsets"][-1])
+    dl.v["hq"][:R].copy_(torch.from_numpy(o["hq"].astype(np.float16)))
+    dl.v["dh"][:R].copy_(torch.from_numpy(o["dh"]))
+    M.moe_down(dl.desc, dl.pack, dl.eoff, dl.ws)
+    torch.cuda.synchronize()
+    assert rel_rms(dl.get("dm", R), o["dm"]) <= TOL_DM
+
+
+# --------------------------------------------------------- full-size layers
+def _sample_rows(R, counts, offsets, order, rng, n=48):
+    rows = set(rng.choice(R, size=min(n, R), replace=False).tolist())
+    big = int(order[0])
+    rows.update([int(offsets[big]), int(offsets[big + 1]) - 1])
+    for e in order[:3]:
+        e = int(e)
+        if counts[e] > 64:
+            rows.update([int(offsets[e]) + 63, int(offsets[e]) + 64])
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+@pytest.mark.parametrize("cfg", [1, 3, 2])
+def test_full_size_config_sampled(M, cfg):
+    """Configurations 1-3 at full size: routing and q8 of x compared in full;
+    GU, Hq, Dm on sampled rows and out on sampled tokens."""
+    L = synth.config_layer(cfg)
+    s = L.shape
+    dl = DeviceLayer(M, L)
+    dl.run_layer()
+    assert dl.status() == 0
+    counts, offsets, row_src, dst_of, bad = oracle.route(L.topk_ids, s.E)
+    assert bad == 0
+    o = dict(counts=counts, offsets=offsets, row_src=row_src, dst_of=dst_of)
+    check_route(dl, o)
+    xq, dx = oracle.quant_q8(L.x)
+    check_q8_x(dl, dict(xq=xq, dx=dx))
+    R = int(offsets[-1])
+    rng = np.random.default_rng(cfg)
+    rows = _sample_rows(R, counts, offsets, dl.get("order"), rng)
+    gu_o, hq_o, dh_o, dm_o, exp = oracle_rows(L, o, xq, dx, rows)
+    gu_g = dl.v["gu"][torch.from_numpy(rows).cuda()].cpu().numpy()
+    assert rel_rms(gu_g, gu_o) <= TOL_GU
+    hq_g = dl.v["hq"][torch.from_numpy(rows).cuda()].cpu().numpy()
+    dh_g = dl.v["dh"][torch.from_numpy(rows).cuda()].cpu().numpy()
+    frac, mx, n = hq_compare(hq_g, hq_o)
+    assert frac <= max(TOL_HQ_FRAC, 2.0 / hq_o.size) and mx <= 1, (frac, mx, n)
+    dm_g = dl.v["dm"][torch.from_numpy(rows).cuda()].cpu().numpy()
+    # the down product alone on the GPU's own Hq
+    dm_ref = oracle_down_rows(L, exp, hq_g.astype(np.int8), dh_g)
+    assert rel_rms(dm_g, dm_ref) <= TOL_DM
+    # out of sampled tokens through the oracle's chain
+    toks = np.array(sorted(set(rng.choice(s.T, size=6, replace=False).tolist()) | {0, s.T - 1}))
+    flat_rows = dst_of.reshape(s.T, s.k)[toks].reshape(-1)
+    _, _, _, dm_t, _ = oracle_rows(L, o, xq, dx, flat_rows)
+    out_ref = np.zeros((len(toks), s.d), np.float32)
+    for i, t in enumerate(toks):
+        out_ref[i] = oracle.combine(L.topk_w[t][None], np.arange(s.k, dtype=np.int32),
+                                    dm_t[i * s.k:(i + 1) * s.k], s.d)[0]
+    out_g = dl.out[torch.from_numpy(toks).cuda()].cpu().numpy()
+    assert rel_rms(out_g, out_ref) <= TOL_OUT
+    assert torch.isfinite(dl.out).all()
+
+
+# ------------------------------------------------------------- edge cases
+def _layer_with_ids(shape, ids, seed=3, x_override=None):
+    L = synth.make_layer(shape, seed=seed, routing="topk",
+                         topk_ids=np.asarray(ids, np.int32).reshape(shape.T, shape.k))
+    if x_override is not None:
+        L.x = np.ascontiguousarray(x_override, np.float32)
+    return L
+
+
+def test_empty_layer(M):
+    shape = synth.LayerShape(0, 256, 64, 8, 2)
+    L = synth.make_layer(shape, seed=1)
+    dl = DeviceLayer(M, L)
+    dl.run_layer()
+    assert dl.status() == 0
+    assert np.array_equal(dl.get("counts"), np.zeros(8, np.int32))
+
+
+def test_single_token_top1(M):
+    shape = synth.LayerShape(1, 256, 64, 4, 1)
+    L = synth.make_layer(shape, seed=2, routing="topk")
+    o = oracle.layer(L)
+    dl = DeviceLayer(M, L)
+    dl.run_layer()
+    check_full(dl, o)
+
+
+def test_expert_row_counts_0_1_65(M):
+    """Experts with 0, 1, 64, 65 and 129 rows (tile boundaries and tails)."""
+    k, E = 1, 6
+    ids = [1] * 1 + [2] * 64 + [3] * 65 + [5] * 129  # experts 0 and 4 empty
+    rng = np.random.default_rng(0)
+    ids = rng.permutation(np.array(ids))
+    shape = synth.LayerShape(len(ids), 256, 128, E, k, synth.W2, synth.W4NL)
+    L = _layer_with_ids(shape, ids)
+    o = oracle.layer(L)
+    dl = DeviceLayer(M, L)
+    dl.run_layer()
+    check_full(dl, o)
+    assert dl.get("counts").tolist() == [0, 1, 64, 65, 0, 129]
+
+
+def test_zero_and_huge_rows(M):
+    """A zero token (every block d = 0, q = 0) and a token with one huge
+    value (its block quantizes the rest to 0)."""
+    shape = synth.LayerShape(40, 256, 64, 8, 2)
+    L = synth.make_layer(shape, seed=4, routing="topk")
+    L.x[3] = 0.0
+    L.x[7, 10] = 3.0e6
+    L.x[9, :32] = 0.0
+    o = oracle.layer(L)
+    dl = DeviceLayer(M, L)
+    dl.run_layer()
+    check_full(dl, o)
+    xq = dl.get("xq")
+    assert np.all(xq[3] == 0) and np.all(dl.get("dx")[3] == 0)
+    assert xq[7, 10] == 127 and np.count_nonzero(xq[7, :32]) == 1
+
+
+def test_bad_expert_id_is_dropped_and_flagged(M):
+    shape = synth.LayerShape(20, 256, 64, 8, 2)
+    L = synth.make_layer(shape, seed=5, routing="topk")
+    L.topk_ids[4, 1] = 8      # out of range
+    L.topk_ids[11, 0] = -3    # out of range
+    o = oracle.layer(L)
+    assert o["bad"] == 2
+    dl = DeviceLayer(M, L)
+    dl.run_layer()
+    st = dl.status()
+    assert st & M.MOE_STATUS_BAD_EXPERT_ID
+    check_full(dl, o)
+
+
+def test_bad_expert_offset_is_skipped_and_flagged(M):
+    shape = synth.LayerShape(16, 256, 64, 4, 1)
+    L = synth.make_layer(shape, seed=6, routing="topk")
+    L.expert_offsets = L.expert_offsets.copy()
+    L.expert_offsets[0, 1] = L.weight_pack.size - 8   # runs past the pack
+    L.expert_offsets[1, 0] += 2                       # misaligned
+    dl = DeviceLayer(M, L)
+    dl.run_layer()
+    assert dl.status() & M.MOE_STATUS_BAD_OFFSET
+
+
+def test_host_buffers_entry_point(M):
+    """moe_prefill_layer_host (host x/ids/w/out) equals the device entry."""
+    L = SMALL["mid_w2_w2"]()
+    dl = DeviceLayer(M, L)
+    dl.run_layer()
+    ref = dl.out.cpu().numpy()
+    hx = torch.from_numpy(L.x).pin_memory()
+    hi = torch.from_numpy(L.topk_ids).pin_memory()
+    hw = torch.from_numpy(L.topk_w).pin_memory()
+    ho = torch.empty((L.shape.T, L.shape.d), dtype=torch.float32).pin_memory()
+    io = torch.empty(M.host_io_bytes(dl.desc), dtype=torch.uint8, device="cuda")
+    M.moe_prefill_layer_host(dl.desc, hx, hi, hw, dl.pack, dl.eoff, ho, io, dl.ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(ho.numpy(), ref)
+
+
+def test_repeat_is_deterministic(M):
+    L = SMALL["mid_w2_w2"]()
+    dl = DeviceLayer(M, L)
+    dl.run_layer()
+    a = dl.out.cpu().numpy().copy()
+    dl.run_layer()
+    assert np.array_equal(dl.out.cpu().numpy(), a)
+
+
+def test_launch_counter_counts(M):
+    L = SMALL["cfg0_tiny"]()
+    dl = DeviceLayer(M, L)
+    n0 = M.moe_kernel_launches()
+    dl.run_layer()
+    assert M.moe_kernel_launches() - n0 >= 6
