@@ -84,8 +84,11 @@ enum {
                                      did not write (stage API misuse): skipped */
 };
 
-/* Supported shapes: T >= 0; d and n_ff multiples of 64, 64 <= d <= 8192,
- * 64 <= n_ff <= 4096; 1 <= E <= 1024; 1 <= k <= E; T*k < 2^24. */
+/* Supported shapes: T >= 0; d a multiple of 128, 128 <= d <= 8192; n_ff a
+ * multiple of 64, 64 <= n_ff <= 4096; 1 <= E <= 1024; 1 <= k <= E;
+ * T*k < 2^24.  Each weight matrix's 128-row tile is staged in shared memory:
+ * either it fits in 45 KB (K <= 1280 for W2, K <= 640 for W4NL) or its K is a
+ * multiple of 512 (W2) / 256 (W4NL).  Other shapes return MOE_ERR_SHAPE. */
 typedef struct MoeLayerDesc {
   int32_t T;        /* tokens                                        */
   int32_t d;        /* hidden size (gate/up K, down output rows)      */
@@ -108,10 +111,13 @@ typedef struct MoeLayerDesc {
  *   order   int32 [E]        expert ids by count, largest first, ties by id
  *   row_src int32 [R]        routed row -> flat entry t*k+r
  *   dst_of  int32 [R]        flat entry -> routed row (-1 if its id is bad)
- *   xq      fp16  [T*d]      q8 values of x as exact fp16 integers
+ *   xq      fp16  [T*d]      q8 values of x as exact fp16 integers, stored
+ *                            pair-interleaved in every 16-value group:
+ *                            position 2i holds value i, 2i+1 holds value i+8
  *   dx      fp32  [T*d/32]   q8 scales of x
  *   gu      fp32  [R*2*n_ff] gate/up rows (gate half, then up half)
- *   hq      fp16  [R*n_ff]   q8 values of H as exact fp16 integers
+ *   hq      fp16  [R*n_ff]   q8 values of H as exact fp16 integers, stored
+ *                            pair-interleaved like xq
  *   dh      fp32  [R*n_ff/32] q8 scales of H
  *   dm      fp32  [R*d]      down rows
  *   status  int32 [1]        MOE_STATUS_* bits */

@@ -62,7 +62,7 @@ Layout layout(const MoeLayerDesc& d) {
 
 int validate_desc(const MoeLayerDesc* d) {
   if (!d) return MOE_ERR_NULL;
-  if (d->T < 0 || d->d < 64 || d->d > 8192 || d->d % 64 != 0 || d->n_ff < 64 ||
+  if (d->T < 0 || d->d < 128 || d->d > 8192 || d->d % 128 != 0 || d->n_ff < 64 ||
       d->n_ff > 4096 || d->n_ff % 64 != 0 || d->E < 1 || d->E > 1024 || d->k < 1 ||
       d->k > d->E)
     return MOE_ERR_SHAPE;
@@ -72,6 +72,8 @@ int validate_desc(const MoeLayerDesc* d) {
       d->gu_layout != MOE_GU_SPLIT || d->flags != 0 || d->reserved != 0)
     return MOE_ERR_FORMAT;
   if (d->weight_pack_bytes < 0) return MOE_ERR_SHAPE;
+  // the product kernel stages each 128-row weight tile in shared memory
+  if (!tc_supported(*d)) return MOE_ERR_SHAPE;
   return MOE_OK;
 }
 
@@ -163,7 +165,7 @@ int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaSt
     a.out = c.v.dm;
     a.act_rows = rows_max(c.d);
   }
-  return launch_rc(launch_gemm(a, st));
+  return launch_rc(launch_gemm_tc(a, a.act, a.act_rows, st));
 }
 
 int run_swiglu(Ctx& c, cudaStream_t st) {

@@ -72,7 +72,10 @@ struct GemmArgs {
   int64_t act_rows;          // rows of act (T for gate/up, T*k for down)
   int32_t* status;
 };
-cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st);
+// tcgen05 product kernel; `act` is the fp16 activation matrix [act_rows x K]
+bool tc_supported(const MoeLayerDesc& d);
+cudaError_t launch_gemm_tc(const GemmArgs& a, const void* act, int64_t act_rows,
+                           cudaStream_t st);
 
 int device_sm_count();
 

@@ -9,7 +9,10 @@
 //
 // Quantised values are stored as exact fp16 integers (|q| <= 127): that is
 // the operand type of the fp16 tensor-core products, and it carries the same
-// information as the int8 code.
+// information as the int8 code.  Within each 16-value group they are stored
+// pair-interleaved (position 2i holds value i, 2i+1 holds value i+8), the
+// order the product kernel's weight decode produces; a permutation inside a
+// 32-value block leaves every block sum unchanged.
 //
 // Every division is IEEE (__fdiv_rn), rounding to integer is rintf (half to
 // even), and the q8 decisions are taken in fp32 exactly as the method states.
@@ -36,7 +39,18 @@ __device__ __forceinline__ float q8_group8(const float (&v)[8], uint4& packed) {
     const __half2 h = __floats2half2_rn(q0, q1);  // exact: |q| <= 127
     w[i] = *reinterpret_cast<const uint32_t*>(&h);
   }
-  packed = make_uint4(w[0], w[1], w[2], w[3]);
+  // Pair-interleave within each 16-value group: this thread (8 values) and
+  // its partner lane (the other 8 values of the group) swap halves so that
+  // stored position 2i holds value i and 2i+1 holds value i+8.
+  const bool first = (threadIdx.x & 1) == 0;  // values 0..7 of the group
+  const uint32_t s0 = first ? w[2] : w[0];
+  const uint32_t s1 = first ? w[3] : w[1];
+  const uint32_t r0 = __shfl_xor_sync(0xffffffffu, s0, 1);
+  const uint32_t r1 = __shfl_xor_sync(0xffffffffu, s1, 1);
+  const uint32_t l0 = first ? w[0] : r0, l1 = first ? w[1] : r1;  // values 0-3 / 4-7 pairs
+  const uint32_t h0 = first ? r0 : w[2], h1 = first ? r1 : w[3];  // values 8-11 / 12-15 pairs
+  packed = make_uint4(__byte_perm(l0, h0, 0x5410), __byte_perm(l0, h0, 0x7632),
+                      __byte_perm(l1, h1, 0x5410), __byte_perm(l1, h1, 0x7632));
   return d;
 }
 

@@ -32,6 +32,24 @@ def require_gpu():
     return M
 
 
+# The library stores q8 values pair-interleaved in each 16-value group:
+# stored position 2i holds value i, 2i+1 holds value i+8.
+_UNPAIR = np.array([2 * (o % 8) + o // 8 for o in range(16)])
+_PAIR = np.array([(p >> 1) + 8 * (p & 1) for p in range(16)])
+
+
+def unpair16(a: np.ndarray) -> np.ndarray:
+    """Stored (pair-interleaved) order -> natural order along the last axis."""
+    sh = a.shape
+    return a.reshape(*sh[:-1], sh[-1] // 16, 16)[..., _UNPAIR].reshape(sh)
+
+
+def pair16(a: np.ndarray) -> np.ndarray:
+    """Natural order -> stored (pair-interleaved) order along the last axis."""
+    sh = a.shape
+    return a.reshape(*sh[:-1], sh[-1] // 16, 16)[..., _PAIR].reshape(sh)
+
+
 def rel_rms(a, b) -> float:
     a = np.asarray(a, np.float64)
     b = np.asarray(b, np.float64)
@@ -84,6 +102,8 @@ class DeviceLayer:
         if rows is not None:
             t = t[:rows]
         a = t.cpu().numpy()
+        if name in ("xq", "hq"):
+            a = unpair16(a)
         return a
 
 

@@ -11,7 +11,7 @@ import oracle
 import synth
 from gpu_harness import (DeviceLayer, TOL_DM, TOL_GU, TOL_HQ_FRAC, TOL_OUT, check_full,
                          check_q8_x, check_route, hq_compare, oracle_down_rows, oracle_rows,
-                         rel_rms, require_gpu)
+                         pair16, rel_rms, require_gpu, unpair16)
 
 pytestmark = pytest.mark.gpu
 
@@ -66,7 +66,7 @@ def test_down_alone_on_oracle_hq(M):
     dl = DeviceLayer(M, L)
     dl.run_layer()
     R = int(o["offsets"][-1])
-    dl.v["hq"][:R].copy_(torch.from_numpy(o["hq"].astype(np.float16)))
+    dl.v["hq"][:R].copy_(torch.from_numpy(pair16(o["hq"]).astype(np.float16)))
     dl.v["dh"][:R].copy_(torch.from_numpy(o["dh"]))
     M.moe_down(dl.desc, dl.pack, dl.eoff, dl.ws)
     torch.cuda.synchronize()
@@ -106,7 +106,7 @@ def test_full_size_config_sampled(M, cfg):
     gu_o, hq_o, dh_o, dm_o, exp = oracle_rows(L, o, xq, dx, rows)
     gu_g = dl.v["gu"][torch.from_numpy(rows).cuda()].cpu().numpy()
     assert rel_rms(gu_g, gu_o) <= TOL_GU
-    hq_g = dl.v["hq"][torch.from_numpy(rows).cuda()].cpu().numpy()
+    hq_g = unpair16(dl.v["hq"][torch.from_numpy(rows).cuda()].cpu().numpy())
     dh_g = dl.v["dh"][torch.from_numpy(rows).cuda()].cpu().numpy()
     frac, mx, n = hq_compare(hq_g, hq_o)
     assert frac <= max(TOL_HQ_FRAC, 2.0 / hq_o.size) and mx <= 1, (frac, mx, n)
