@@ -111,14 +111,18 @@ typedef struct MoeLayerDesc {
  *   order   int32 [E]        expert ids by count, largest first, ties by id
  *   row_src int32 [R]        routed row -> flat entry t*k+r
  *   dst_of  int32 [R]        flat entry -> routed row (-1 if its id is bad)
- *   xq      fp16  [T*d]      q8 values of x as exact fp16 integers, stored
- *                            pair-interleaved in every 16-value group:
- *                            position 2i holds value i, 2i+1 holds value i+8
- *   dx      fp32  [T*d/32]   q8 scales of x
+ *   xq      fp16  [R*d]      q8 values of x as exact fp16 integers, one row
+ *                            per routed row (row r holds token row_src[r]/k:
+ *                            quantize and scatter), stored pair-interleaved in
+ *                            every 16-value group: position 2i holds value i,
+ *                            2i+1 holds value i+8
+ *   dx      fp32  [R*sd]     q8 scales of x per routed row, rows padded to
+ *                            sd = d/32 rounded up to a multiple of 4
  *   gu      fp32  [R*2*n_ff] gate/up rows (gate half, then up half)
  *   hq      fp16  [R*n_ff]   q8 values of H as exact fp16 integers, stored
  *                            pair-interleaved like xq
- *   dh      fp32  [R*n_ff/32] q8 scales of H
+ *   dh      fp32  [R*sf]     q8 scales of H, rows padded to sf = n_ff/32
+ *                            rounded up to a multiple of 4
  *   dm      fp32  [R*d]      down rows
  *   status  int32 [1]        MOE_STATUS_* bits */
 typedef struct MoeWorkspaceView {

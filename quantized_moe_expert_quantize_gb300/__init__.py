@@ -175,11 +175,12 @@ def workspace_view(desc: MoeLayerDesc, ws: torch.Tensor) -> dict:
     base = ws.data_ptr()
     T, d, n_ff, E, k = desc.T, desc.d, desc.n_ff, desc.E, desc.k
     R = T * k
+    ssd, ssf = ((d // 32) + 3) // 4 * 4, ((n_ff // 32) + 3) // 4 * 4  # padded scale rows
     spec = dict(counts=((E,), torch.int32), offsets=((E + 1,), torch.int32),
                 order=((E,), torch.int32), row_src=((R,), torch.int32),
-                dst_of=((R,), torch.int32), xq=((T, d), torch.float16),
-                dx=((T, d // 32), torch.float32), gu=((R, 2 * n_ff), torch.float32),
-                hq=((R, n_ff), torch.float16), dh=((R, n_ff // 32), torch.float32),
+                dst_of=((R,), torch.int32), xq=((R, d), torch.float16),
+                dx=((R, ssd), torch.float32), gu=((R, 2 * n_ff), torch.float32),
+                hq=((R, n_ff), torch.float16), dh=((R, ssf), torch.float32),
                 dm=((R, d), torch.float32), status=((1,), torch.int32))
     out = {}
     for name, (shape, dt) in spec.items():

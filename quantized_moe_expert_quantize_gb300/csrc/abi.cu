@@ -27,7 +27,7 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t status, counts, offsets, order, row_src, dst_of, hist, xq, dx, gu, hq, dh, dm;
+  size_t status, counts, offsets, order, tiles, row_src, dst_of, hist, xq, dx, gu, hq, dh, dm;
   size_t total;
 };
 
@@ -47,14 +47,15 @@ Layout layout(const MoeLayerDesc& d) {
   L.counts = take(sizeof(int32_t) * d.E);
   L.offsets = take(sizeof(int32_t) * (d.E + 1));
   L.order = take(sizeof(int32_t) * d.E);
+  L.tiles = take(sizeof(int4) * (size_t)max_tiles(R, d.E));
   L.row_src = take(sizeof(int32_t) * R);
   L.dst_of = take(sizeof(int32_t) * R);
   L.hist = take(sizeof(int32_t) * (size_t)nchunks * d.E);
-  L.xq = take(sizeof(uint16_t) * (size_t)d.T * d.d);
-  L.dx = take(sizeof(float) * (size_t)d.T * (d.d / kQBlock));
+  L.xq = take(sizeof(uint16_t) * (size_t)R * d.d);
+  L.dx = take(sizeof(float) * (size_t)R * scale_stride(d.d));
   L.gu = take(sizeof(float) * (size_t)R * 2 * d.n_ff);
   L.hq = take(sizeof(uint16_t) * (size_t)R * d.n_ff);
-  L.dh = take(sizeof(float) * (size_t)R * (d.n_ff / kQBlock));
+  L.dh = take(sizeof(float) * (size_t)R * scale_stride(d.n_ff));
   L.dm = take(sizeof(float) * (size_t)R * d.d);
   L.total = p;
   return L;
@@ -127,11 +128,12 @@ int run_route(Ctx& c, const int32_t* ids, cudaStream_t st) {
   if (cudaMemsetAsync(c.v.status, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_LAUNCH;
   return launch_rc(launch_route(ids, rows_max(c.d), c.d.E, (int32_t*)(c.ws + c.L.hist),
                                 c.v.counts, c.v.offsets, c.v.order, c.v.row_src, c.v.dst_of,
-                                c.v.status, st));
+                                (int4*)(c.ws + c.L.tiles), c.v.status + 1, c.v.status, st));
 }
 
 int run_quant(Ctx& c, const float* x, cudaStream_t st) {
-  return launch_rc(launch_quant_q8(x, c.d.T, c.d.d, (__half*)c.v.xq, c.v.dx, st));
+  return launch_rc(launch_quant_q8(x, c.d.T, c.d.d, c.d.k, c.v.dst_of, rows_max(c.d),
+                                  (__half*)c.v.xq, c.v.dx, st));
 }
 
 int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaStream_t st) {
@@ -144,28 +146,25 @@ int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaSt
   a.counts = c.v.counts;
   a.offsets = c.v.offsets;
   a.order = c.v.order;
+  a.tiles = (const int4*)(c.ws + c.L.tiles);
+  a.ntiles = c.v.status + 1;
   a.E = c.d.E;
-  a.k_top = c.d.k;
   a.status = c.v.status;
   a.rows_max = rows_max(c.d);
   if (which == 0) {
     a.act = (const __half*)c.v.xq;
     a.act_d = c.v.dx;
-    a.row_src = c.v.row_src;
     a.K = c.d.d;
     a.N_out = 2 * c.d.n_ff;
     a.out = c.v.gu;
-    a.act_rows = c.d.T;
   } else {
     a.act = (const __half*)c.v.hq;
     a.act_d = c.v.dh;
-    a.row_src = nullptr;
     a.K = c.d.n_ff;
     a.N_out = c.d.d;
     a.out = c.v.dm;
-    a.act_rows = rows_max(c.d);
   }
-  return launch_rc(launch_gemm_tc(a, a.act, a.act_rows, st));
+  return launch_rc(launch_gemm_tc(a, a.act, st));
 }
 
 int run_swiglu(Ctx& c, cudaStream_t st) {

@@ -15,6 +15,10 @@ constexpr int kW2Values = 64;         // values per W2 block
 constexpr int kW4Values = 32;         // values per W4NL block
 constexpr int kQBlock = 32;           // q8 block of activations
 
+// Row stride (in floats) of a q8 scale matrix [rows x K/32]: padded to a
+// multiple of 4 so every row starts 16-byte aligned (tensor-map rule).
+__host__ __device__ inline int scale_stride(int K) { return ((K / 32) + 3) & ~3; }
+
 __host__ __device__ inline int block_values(int fmt) { return fmt == MOE_FMT_W2 ? kW2Values : kW4Values; }
 __host__ __device__ inline int64_t row_bytes(int fmt, int K) {
   return (int64_t)(K / block_values(fmt)) * kBlockBytes;
@@ -37,14 +41,23 @@ constexpr int kRouteChunk = 1024;  // flat entries per warp
 constexpr int kRouteWarps = 8;     // warps per CTA
 inline int route_chunks(int64_t n) { return (int)((n + kRouteChunk - 1) / kRouteChunk); }
 
+// Routed-row tiles of the product kernels: experts in largest-first order,
+// each expert's rows cut into tiles of at most kTileRows rows.
+constexpr int kTileRows = 128;
+__host__ __device__ inline int64_t max_tiles(int64_t rows, int E) { return rows / kTileRows + E + 1; }
+
+// tiles: int4 {expert, first routed row, rows, 0} [max_tiles]; ntiles: int32 [1]
 cudaError_t launch_route(const int32_t* ids, int64_t n, int E, int32_t* hist,
                          int32_t* counts, int32_t* offsets, int32_t* order,
-                         int32_t* row_src, int32_t* dst_of, int32_t* status,
-                         cudaStream_t st);
+                         int32_t* row_src, int32_t* dst_of, int4* tiles, int32_t* ntiles,
+                         int32_t* status, cudaStream_t st);
 
 // ---------------------------------------------------- elementwise kernels
-cudaError_t launch_quant_q8(const float* x, int64_t rows, int K, __half* q, float* d,
-                            cudaStream_t st);
+// q8 of x [T x K], scattered to routed rows: q [rows_max x K],
+// d [rows_max x scale_stride(K)]
+cudaError_t launch_quant_q8(const float* x, int64_t T, int K, int k, const int32_t* dst_of,
+                            int64_t rows_max, __half* q, float* d, cudaStream_t st);
+// swiglu + q8 of GU [rows x 2 n_ff]: hq [rows_max x n_ff], dh [rows_max x scale_stride(n_ff)]
 cudaError_t launch_swiglu_quant(const float* gu, const int32_t* nrows_dev, int64_t rows_max,
                                 int n_ff, __half* hq, float* dh, cudaStream_t st);
 cudaError_t launch_combine(const float* topk_w, const int32_t* dst_of, const float* dm,
@@ -60,22 +73,21 @@ struct GemmArgs {
   const int32_t* counts;     // [E]
   const int32_t* offsets;    // [E+1]
   const int32_t* order;      // [E] largest first
+  const int4* tiles;         // routed-row tiles, largest expert first
+  const int32_t* ntiles;
   int E;
   const __half* act;         // activation values (exact fp16 integers)
-  const float* act_d;        // activation scales, one per 32 values
-  const int32_t* row_src;    // gather: routed row -> flat entry (token = entry / k_top); null = no gather
-  int k_top;
+  const float* act_d;        // activation scales [rows_max x scale_stride(K)]
   int K;                     // reduction length
   int N_out;                 // output columns (weight rows)
   float* out;                // [rows x N_out]
   int64_t rows_max;          // capacity of the routed-row buffers (T*k)
-  int64_t act_rows;          // rows of act (T for gate/up, T*k for down)
   int32_t* status;
 };
-// tcgen05 product kernel; `act` is the fp16 activation matrix [act_rows x K]
+// tcgen05 product kernel; `act` is the fp16 activation matrix [rows_max x K]
+// in routed-row order
 bool tc_supported(const MoeLayerDesc& d);
-cudaError_t launch_gemm_tc(const GemmArgs& a, const void* act, int64_t act_rows,
-                           cudaStream_t st);
+cudaError_t launch_gemm_tc(const GemmArgs& a, const void* act, cudaStream_t st);
 
 int device_sm_count();
 

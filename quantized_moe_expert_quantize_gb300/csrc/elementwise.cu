@@ -1,7 +1,10 @@
 // Bandwidth-bound steps of the layer:
 //   quant_q8      -- x -> q8 per 32-value block ("Strata #3752", commit
 //                    "swiglu_quant": quantize_mmq_q8_1; layer spec, tiny
-//                    configuration: d = amax/127, q = rint(x/d), d = 0 -> 0);
+//                    configuration: d = amax/127, q = rint(x/d), d = 0 -> 0),
+//                    scattered to the token's k routed rows (quantize_scatter,
+//                    "Strata #3752" commits "moe_ws wiring"), so the product
+//                    kernels read contiguous per-expert row ranges;
 //   swiglu_quant  -- H = silu(g)*u and its q8 in one pass, H never stored
 //                    ("Strata #3752", commit "swiglu_quant");
 //   combine       -- out[t] = sum over ranks r = 0..k-1 of w[t,r]*Dm[row]
@@ -54,9 +57,13 @@ __device__ __forceinline__ float q8_group8(const float (&v)[8], uint4& packed) {
   return d;
 }
 
+// Routed-row layout of the product inputs: values [R x K] fp16 (row r =
+// routed row r), scales [R x scale_stride(K)] (rows padded to 16 bytes), so
+// a product tile's rows are one contiguous range of both.
 __global__ void __launch_bounds__(256)
-quant_q8_kernel(const float* __restrict__ x, int64_t groups, __half* __restrict__ q,
-                float* __restrict__ d) {
+quant_q8_kernel(const float* __restrict__ x, int64_t groups, int K, int k,
+                const int32_t* __restrict__ dst_of, int64_t rows_max,
+                __half* __restrict__ q, float* __restrict__ d) {
   const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const bool ok = g < groups;  // groups is a multiple of 4: quads are whole
   float v[8];
@@ -72,8 +79,16 @@ quant_q8_kernel(const float* __restrict__ x, int64_t groups, __half* __restrict_
   uint4 packed;
   const float db = q8_group8(v, packed);
   if (ok) {
-    reinterpret_cast<uint4*>(q)[g] = packed;
-    if ((g & 3) == 0) d[g >> 2] = db;
+    const int per_row = K / 8;
+    const int64_t t = g / per_row;
+    const int c = (int)(g - t * per_row);
+    const int blk = c >> 2;
+    for (int r = 0; r < k; r++) {
+      const int32_t dst = dst_of[t * k + r];
+      if (dst < 0 || dst >= rows_max) continue;  // dropped (bad expert id)
+      reinterpret_cast<uint4*>(q + (int64_t)dst * K)[c] = packed;
+      if ((c & 3) == 0) d[(int64_t)dst * scale_stride(K) + blk] = db;
+    }
   }
 }
 
@@ -109,7 +124,11 @@ swiglu_quant_kernel(const float* __restrict__ gu, const int32_t* __restrict__ nr
   const float db = q8_group8(v, packed);
   if (ok) {
     reinterpret_cast<uint4*>(hq)[g] = packed;
-    if ((g & 3) == 0) dh[g >> 2] = db;
+    if ((g & 3) == 0) {
+      const int64_t row = g / per_row;
+      const int blk = (int)(g - row * per_row) >> 2;
+      dh[row * scale_stride(n_ff) + blk] = db;
+    }
   }
 }
 
@@ -142,11 +161,12 @@ inline unsigned blocks_for(int64_t threads, int per_block) {
 
 }  // namespace
 
-cudaError_t launch_quant_q8(const float* x, int64_t rows, int K, __half* q, float* d,
-                            cudaStream_t st) {
-  const int64_t groups = rows * (K / 8);
+cudaError_t launch_quant_q8(const float* x, int64_t T, int K, int k, const int32_t* dst_of,
+                            int64_t rows_max, __half* q, float* d, cudaStream_t st) {
+  const int64_t groups = T * (K / 8);
   if (groups == 0) return cudaSuccess;
-  quant_q8_kernel<<<blocks_for(groups, 256), 256, 0, st>>>(x, groups, q, d);
+  quant_q8_kernel<<<blocks_for(groups, 256), 256, 0, st>>>(x, groups, K, k, dst_of, rows_max, q,
+                                                            d);
   count_launch();
   return cudaGetLastError();
 }

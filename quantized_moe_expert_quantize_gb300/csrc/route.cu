@@ -8,9 +8,10 @@
 //                       chunk's rows per expert (shared-memory histogram);
 //   2. route_scan    -- one CTA turns the [chunk][expert] counts into the
 //                       base row of every (chunk, expert), the expert counts,
-//                       their exclusive prefix sum (group bounds) and the
-//                       largest-first expert order used by the product
-//                       kernels' schedulers;
+//                       their exclusive prefix sum (group bounds), the
+//                       largest-first expert order, and the product kernels'
+//                       work list: every expert's rows cut into tiles of at
+//                       most 128 rows, largest expert first;
 //   3. route_scatter -- each warp walks its chunk again, 32 entries at a
 //                       time; __match_any_sync groups lanes of equal expert,
 //                       a lane's rank among them keeps flat order, so rows of
@@ -45,32 +46,16 @@ route_hist_kernel(const int32_t* __restrict__ ids, int64_t n, int E, int nchunks
   for (int e = lane; e < E; e += 32) hist[(int64_t)chunk * E + e] = h[e];
 }
 
-// One CTA of 1024 threads; thread e owns expert e (E <= 1024).
-__global__ void __launch_bounds__(1024)
-route_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E,
-                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                  int32_t* __restrict__ order) {
-  __shared__ int32_t s_cnt[1024];
-  __shared__ int32_t s_warp[32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int run = 0;
-  if (tid < E) {
-    for (int c = 0; c < nchunks; c++) {
-      const int64_t idx = (int64_t)c * E + tid;
-      const int v = hist[idx];
-      hist[idx] = run;  // rows of expert tid in chunks before c
-      run += v;
-    }
-    counts[tid] = run;
-  }
-  s_cnt[tid] = run;
-  // exclusive prefix sum of the counts over the CTA
-  int incl = run;
+// Exclusive prefix sum over the 1024 threads of the CTA (one value each).
+__device__ __forceinline__ int block_excl_scan(int v, int32_t* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
+  __syncthreads();  // s_warp free for reuse
   if (lane == 31) s_warp[warp] = incl;
   __syncthreads();
   if (warp == 0) {
@@ -84,18 +69,57 @@ route_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E,
     s_warp[lane] = wi - w;
   }
   __syncthreads();
-  const int excl = s_warp[warp] + incl - run;
+  return s_warp[warp] + incl - v;
+}
+
+// One CTA of 1024 threads; thread e owns expert e (E <= 1024).
+__global__ void __launch_bounds__(1024)
+route_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E,
+                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                  int32_t* __restrict__ order, int4* __restrict__ tiles,
+                  int32_t* __restrict__ ntiles) {
+  __shared__ int32_t s_cnt[1024];    // rows of expert e
+  __shared__ int32_t s_tiles[1024];  // tiles of the expert at rank r
+  __shared__ int32_t s_warp[32];
+  const int tid = threadIdx.x;
+  int run = 0;
+  if (tid < E) {
+    for (int c = 0; c < nchunks; c++) {
+      const int64_t idx = (int64_t)c * E + tid;
+      const int v = hist[idx];
+      hist[idx] = run;  // rows of expert tid in chunks before c
+      run += v;
+    }
+    counts[tid] = run;
+  }
+  s_cnt[tid] = run;
+  s_tiles[tid] = 0;
+  const int excl = block_excl_scan(run, s_warp);  // also orders s_cnt / s_tiles writes
+  int rank = 0;
   if (tid < E) {
     offsets[tid] = excl;
     if (tid == E - 1) offsets[E] = excl + run;
     for (int c = 0; c < nchunks; c++) hist[(int64_t)c * E + tid] += excl;
     // rank by (count descending, id ascending)
-    int r = 0;
     for (int e2 = 0; e2 < E; e2++) {
       const int c2 = s_cnt[e2];
-      r += (c2 > run) || (c2 == run && e2 < tid);
+      rank += (c2 > run) || (c2 == run && e2 < tid);
     }
-    order[r] = tid;
+    order[rank] = tid;
+    s_tiles[rank] = (run + kTileRows - 1) / kTileRows;
+  }
+  __syncthreads();
+  // first tile of each rank (thread tid stands for rank tid here)
+  const int nt = s_tiles[tid];
+  const int tbase = block_excl_scan(nt, s_warp);
+  if (tid == 1023) *ntiles = tbase + nt;
+  __syncthreads();
+  s_tiles[tid] = tbase;
+  __syncthreads();
+  if (tid < E) {
+    const int first = s_tiles[rank];
+    for (int i = 0; i * kTileRows < run; i++)
+      tiles[first + i] = make_int4(tid, excl + i * kTileRows, min(kTileRows, run - i * kTileRows), 0);
   }
 }
 
@@ -133,8 +157,8 @@ route_scatter_kernel(const int32_t* __restrict__ ids, int64_t n, int E, int nchu
 
 cudaError_t launch_route(const int32_t* ids, int64_t n, int E, int32_t* hist,
                          int32_t* counts, int32_t* offsets, int32_t* order,
-                         int32_t* row_src, int32_t* dst_of, int32_t* status,
-                         cudaStream_t st) {
+                         int32_t* row_src, int32_t* dst_of, int4* tiles, int32_t* ntiles,
+                         int32_t* status, cudaStream_t st) {
   const int nchunks = route_chunks(n);
   const int grid = (nchunks + kRouteWarps - 1) / kRouteWarps;
   const size_t smem = sizeof(int32_t) * kRouteWarps * E;
@@ -142,7 +166,8 @@ cudaError_t launch_route(const int32_t* ids, int64_t n, int E, int32_t* hist,
     route_hist_kernel<<<grid, kRouteWarps * 32, smem, st>>>(ids, n, E, nchunks, hist, status);
     count_launch();
   }
-  route_scan_kernel<<<1, 1024, 0, st>>>(hist, nchunks, E, counts, offsets, order);
+  route_scan_kernel<<<1, 1024, 0, st>>>(hist, nchunks, E, counts, offsets, order, tiles,
+                                        ntiles);
   count_launch();
   if (grid > 0) {
     route_scatter_kernel<<<grid, kRouteWarps * 32, smem, st>>>(ids, n, E, nchunks, hist,

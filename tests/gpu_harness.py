@@ -98,10 +98,16 @@ class DeviceLayer:
         return self.M.moe_read_status(self.desc, self.ws)
 
     def get(self, name, rows=None) -> np.ndarray:
+        """A workspace region as numpy, in natural order: q8 values
+        un-interleaved, scale rows without their padding."""
         t = self.v[name]
+        if name == "dx":
+            t = t[:, : self.L.shape.d // 32]
+        if name == "dh":
+            t = t[:, : self.L.shape.n_ff // 32]
         if rows is not None:
             t = t[:rows]
-        a = t.cpu().numpy()
+        a = t.contiguous().cpu().numpy()
         if name in ("xq", "hq"):
             a = unpair16(a)
         return a
@@ -121,9 +127,20 @@ def check_route(dl: DeviceLayer, o: dict):
 
 
 def check_q8_x(dl: DeviceLayer, o: dict):
-    xq = dl.get("xq").astype(np.float32)
-    assert np.array_equal(xq, o["xq"].astype(np.float32))
-    assert np.array_equal(dl.get("dx"), o["dx"])
+    """q8 of x, scattered to routed rows: row r holds token row_src[r] // k.
+    Compared bit for bit on the device (the full-size layers are large)."""
+    k = dl.L.shape.k
+    row_src = torch.from_numpy(np.ascontiguousarray(o["row_src"])).long().cuda()
+    R = row_src.numel()
+    tok = row_src // k
+    want_q = torch.from_numpy(np.ascontiguousarray(o["xq"])).cuda()[tok].to(torch.float16)
+    got_q = dl.v["xq"][:R]
+    perm = torch.from_numpy(_UNPAIR).cuda()
+    got_q = got_q.view(R, -1, 16)[:, :, perm].reshape(R, -1)
+    assert torch.equal(got_q, want_q), "q8 values of x differ from the oracle"
+    want_d = torch.from_numpy(np.ascontiguousarray(o["dx"])).cuda()[tok]
+    got_d = dl.v["dx"][:R, : dl.L.shape.d // 32]
+    assert torch.equal(got_d, want_d), "q8 scales of x differ from the oracle"
 
 
 def hq_compare(hq_gpu: np.ndarray, hq_ref: np.ndarray):

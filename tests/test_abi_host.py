@@ -43,7 +43,8 @@ def test_workspace_bytes_layout(lib):
     d = M.make_desc(16384, 2560, 640, 512, 10)
     n = M.workspace_bytes(d)
     R = 16384 * 10
-    minimum = R * (2 * 640 * 4 + 640 * 2 + 640 // 32 * 4 + 2560 * 4 + 8) + 16384 * 2560 * 2
+    # per routed row: gu, hq, dh, dm, row_src + dst_of, scattered xq and dx
+    minimum = R * (2 * 640 * 4 + 640 * 2 + 20 * 4 + 2560 * 4 + 8 + 2560 * 2 + 80 * 4)
     assert minimum <= n <= minimum + 64 * 2**20
     assert n % 256 == 0
     assert M.host_io_bytes(d) >= 2 * 16384 * 2560 * 4
