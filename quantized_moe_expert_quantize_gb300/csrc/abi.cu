@@ -27,7 +27,8 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t status, counts, offsets, order, tiles, row_src, dst_of, hist, xq, dx, gu, hq, dh, dm;
+  size_t status, counts, offsets, order, tiles, tmaps, row_src, dst_of, hist, xq, dx, gu, hq, dh,
+      dm;
   size_t total;
 };
 
@@ -48,6 +49,7 @@ Layout layout(const MoeLayerDesc& d) {
   L.offsets = take(sizeof(int32_t) * (d.E + 1));
   L.order = take(sizeof(int32_t) * d.E);
   L.tiles = take(sizeof(int4) * (size_t)max_tiles(R, d.E));
+  L.tmaps = take(kTmapSlotBytes);
   L.row_src = take(sizeof(int32_t) * R);
   L.dst_of = take(sizeof(int32_t) * R);
   L.hist = take(sizeof(int32_t) * (size_t)nchunks * d.E);
@@ -164,7 +166,7 @@ int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaSt
     a.N_out = c.d.d;
     a.out = c.v.dm;
   }
-  return launch_rc(launch_gemm_tc(a, a.act, st));
+  return launch_rc(launch_gemm_tc(a, a.act, c.ws + c.L.tmaps, st));
 }
 
 int run_swiglu(Ctx& c, cudaStream_t st) {

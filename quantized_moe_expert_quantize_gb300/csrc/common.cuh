@@ -87,7 +87,10 @@ struct GemmArgs {
 // tcgen05 product kernel; `act` is the fp16 activation matrix [rows_max x K]
 // in routed-row order
 bool tc_supported(const MoeLayerDesc& d);
-cudaError_t launch_gemm_tc(const GemmArgs& a, const void* act, cudaStream_t st);
+// tmap_slots: global scratch for per-CTA tensor maps, kTmapSlotBytes
+constexpr size_t kTmapSlotBytes = 1024 * 2 * 128;
+cudaError_t launch_gemm_tc(const GemmArgs& a, const void* act, uint8_t* tmap_slots,
+                           cudaStream_t st);
 
 int device_sm_count();
 

@@ -40,9 +40,11 @@
 //   warps 8-11  weight decode: raw blocks (bulk-copied to shared memory)
 //               -> fp16 operand tile in the 128-byte swizzle layout, once
 //               per tile
-//   warp 12     producer: bulk TMA of raw weight bytes, one 2-D TMA box of
-//               the tile's 128 activation rows (routed-row order) and one of
-//               their scales per stage
+//   warp 12     producer: raw weight bytes by TMA (a tensor map retargeted
+//               per expert on the device: one 2-D box of 128 rows x 8 blocks
+//               per chunk, or one bulk copy of a whole small tile), one 2-D
+//               TMA box of the tile's 128 activation rows (routed-row order)
+//               and one of their scales per stage
 //   warp 13     MMA issue (one thread) and TMEM allocation
 //   warps 14-15 idle
 // Activations arrive in routed-row order (the q8 and swiglu_quant steps
@@ -54,6 +56,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -76,6 +79,7 @@ constexpr int kWarpProducer = 12;
 constexpr int kWarpMma = 13;
 constexpr uint32_t kTmemCols = 512;  // four buffers x 128 fp32 columns
 constexpr uint64_t kTimeoutNs = 1000000000ull;
+constexpr int kMaxGrid = 1024;   // CTAs; each owns two 128-byte tensor-map slots
 
 constexpr int kScaleBox = 4;    // scale columns (32-value blocks) per TMA box: 16 bytes a row
 constexpr int kABytes = kM * kSK * 2;     // weight operand per stage: 16 KB
@@ -91,8 +95,10 @@ constexpr int kOffBar = kOffDw + kStages * 2 * kM * 4;
 constexpr int kNumBars = 3 * kStages + 2 * kTBufs + 2 + 2 + 1;
 constexpr int kOffEoff = kOffBar + kNumBars * 8;  // int64 [E] weight offsets of this product
 constexpr int kOffMisc = kOffEoff + 1024 * 8;
-constexpr int kSmemBytes = kOffMisc + 256 + 1024;  // misc words + alignment slack
+constexpr int kOffTmap = (kOffMisc + 256 + 127) & ~127;  // two 128-byte weight tensor maps
+constexpr int kSmemBytes = kOffTmap + 256 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a CTA can have");
+static_assert(kOffTmap % 128 == 0 && kOffBar % 8 == 0 && kOffEoff % 8 == 0, "alignment");
 
 struct TcArgs {
   const uint8_t* pack;
@@ -113,6 +119,7 @@ struct TcArgs {
   float* out;
   int64_t rows_max;
   int32_t* status;
+  uint8_t* tmap_slots;  // per CTA: two 128-byte global slots for the weight tensor map
 };
 
 struct Item {
@@ -230,7 +237,8 @@ __device__ __forceinline__ float decode_w4_store(const uint8_t* blk, const uint1
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
-               const __grid_constant__ CUtensorMap tmap_d) {
+               const __grid_constant__ CUtensorMap tmap_d,
+               const __grid_constant__ CUtensorMap tmap_w) {
   constexpr bool kFold = (FMT == MOE_FMT_W2);
 
   extern __shared__ uint8_t smem_raw[];
@@ -324,11 +332,11 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
   {                                                                                      \
     const uint32_t st_ = (it + (b) / 2) % kStages, ph_ = ((it + (b) / 2) / kStages) & 1; \
     if (((b) & 1) == 0) {                                                                \
-      alive = mbar_wait(&full_tma[st_], ph_, s_abort, kTimeoutNs);                       \
-      if (!kFold && alive) alive = mbar_wait(&full_dec[st_], ph_, s_abort, kTimeoutNs); \
+      alive = mbar_wait(&full_tma[st_], ph_, s_abort, kTimeoutNs, false);                       \
+      if (!kFold && alive) alive = mbar_wait(&full_dec[st_], ph_, s_abort, kTimeoutNs, false); \
     }                                                                                    \
     const uint32_t n_ = bc + (b), buf_ = n_ % kTBufs;                                     \
-    if (alive) alive = mbar_wait(&tfull[buf_], (n_ / kTBufs) & 1, s_abort, kTimeoutNs);  \
+    if (alive) alive = mbar_wait(&tfull[buf_], (n_ / kTBufs) & 1, s_abort, kTimeoutNs, false);  \
     tc_fence_after();                                                                    \
     if (alive && active) {                                                               \
       tmem_ld32x2(tlane + buf_ * kM, (v));                                               \
@@ -455,7 +463,13 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
     const int bps = (FMT == MOE_FMT_W2) ? 1 : 2;  // blocks per stage
     int64_t r_item = blockIdx.x;
     int r_chunk = 0;
-    uint32_t issued = 0;
+    uint32_t issued = 0, r_items = 0;  // raw chunks issued, items whose raw stream began
+    uint8_t* s_tmap = smem + kOffTmap;  // two copies of the weight tensor-map template
+    if (a.rows_mode) {
+      for (int i = lane; i < 64; i += 32)
+        reinterpret_cast<uint32_t*>(s_tmap)[i] = reinterpret_cast<const uint32_t*>(&tmap_w)[i & 31];
+      __syncwarp();
+    }
     Item RI;
     auto seek_raw = [&]() -> bool {
       while (r_item < total) {
@@ -472,23 +486,30 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
       if (!mbar_wait(&rempty[slot], ((issued / a.raw_slots) & 1) ^ 1, s_abort, kTimeoutNs))
         return false;
       const int s0 = r_chunk * spc;
-      const int ns = min(spc, nstages - s0);
-      const int row_bytes = a.rows_mode ? ns * bps * kBlockBytes : (int)a.pitch;
+      const int row_bytes = a.rows_mode ? a.chunk_row_bytes : (int)a.pitch;
       const uint32_t bytes = (uint32_t)(row_bytes * kM);
       uint8_t* dst = sRaw + slot * kRawSlot;
-      if (lane == 0) mbar_arrive_expect_tx(&rfull[slot], bytes);
-      __syncwarp();
-      if (a.rows_mode) {
-        const uint8_t* src = RI.wbase + (int64_t)s0 * bps * kBlockBytes;
-        for (int row = lane; row < kM; row += 32)
-          bulk_g2s(dst + row * a.chunk_row_bytes, src + row * a.pitch, (uint32_t)row_bytes,
-                   &rfull[slot]);
-      } else if (lane == 0) {
-        bulk_g2s(dst, RI.wbase, bytes, &rfull[slot]);
+      uint8_t* gslot = a.tmap_slots + ((int64_t)blockIdx.x * 2 + (r_items & 1)) * 128;
+      if (a.rows_mode && r_chunk == 0) {
+        // point this item's weight tensor map (slots ping-pong per item) at
+        // the expert's matrix; its previous user, two items back, has landed
+        uint8_t* sm = s_tmap + 128 * (r_items & 1);
+        if (lane == 0) tmap_replace_address(sm, RI.wbase - (int64_t)RI.o0 * a.pitch);
+        __syncwarp();
+        tmap_publish(gslot, sm);
       }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&rfull[slot], bytes);
+        if (a.rows_mode)  // 128 weight rows x one chunk of 8 blocks: one 2-D box
+          tma_load_2d(dst, gslot, s0 * bps * kBlockBytes, RI.o0, &rfull[slot]);
+        else  // the whole contiguous 128-row tile: one bulk copy
+          bulk_g2s(dst, RI.wbase, bytes, &rfull[slot]);
+      }
+      __syncwarp();
       issued++;
       if (++r_chunk == chunks_per_item) {
         r_chunk = 0;
+        r_items++;
         r_item += stride;
         r_valid = seek_raw();
       }
@@ -534,8 +555,8 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
         for (int s = 0; s < nstages && alive; s++, it++) {
           const int st = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
-          if (!mbar_wait(&full_tma[st], ph, s_abort, kTimeoutNs) ||
-              !mbar_wait(&full_dec[st], ph, s_abort, kTimeoutNs)) {
+          if (!mbar_wait(&full_tma[st], ph, s_abort, kTimeoutNs, false) ||
+              !mbar_wait(&full_dec[st], ph, s_abort, kTimeoutNs, false)) {
             alive = false;
             break;
           }
@@ -544,7 +565,7 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
           const uint32_t xaddr = smem_u32(sB + st * kBBytes);  // routed rows: MMA A operand
           for (int kb = 0; kb < 2; kb++) {
             const uint32_t buf = bc % kTBufs;
-            if (!mbar_wait(&tempty[buf], ((bc / kTBufs) & 1) ^ 1, s_abort, kTimeoutNs)) {
+            if (!mbar_wait(&tempty[buf], ((bc / kTBufs) & 1) ^ 1, s_abort, kTimeoutNs, false)) {
               alive = false;
               break;
             }
@@ -643,7 +664,8 @@ bool tc_supported(const MoeLayerDesc& d) {
          tc_raw_plan(d.down_fmt, d.n_ff, &p, &crb, &spc, &rs, &rm);
 }
 
-cudaError_t launch_gemm_tc(const GemmArgs& g, const void* act, cudaStream_t st) {
+cudaError_t launch_gemm_tc(const GemmArgs& g, const void* act, uint8_t* tmap_slots,
+                           cudaStream_t st) {
   if (g.rows_max == 0) return cudaSuccess;
   TcArgs a{};
   a.pack = g.pack;
@@ -684,15 +706,31 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, const void* act, cudaStream_t st) 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
 
+  // weight tensor-map template for rows mode: [N_out rows x pitch bytes],
+  // boxes of 128 rows x one chunk; the kernel retargets its base per expert
+  CUtensorMap tmap_w;
+  std::memset(&tmap_w, 0, sizeof(tmap_w));
+  if (a.rows_mode) {
+    const cuuint64_t wdims[2] = {(cuuint64_t)a.pitch, (cuuint64_t)g.N_out};
+    const cuuint64_t wstrides[1] = {(cuuint64_t)a.pitch};
+    const cuuint32_t wbox[2] = {(cuuint32_t)a.chunk_row_bytes, (cuuint32_t)kM};
+    if (encode(&tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(g.pack), wdims,
+               wstrides, wbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  a.tmap_slots = tmap_slots;
+
   const int64_t tiles_max = max_tiles(g.rows_max, g.E) * (int64_t)(g.N_out / kM);
-  const int grid = (int)std::min<int64_t>(tiles_max, device_sm_count());
+  const int grid = (int)std::min<int64_t>(std::min<int64_t>(tiles_max, device_sm_count()),
+                                          kMaxGrid);
   cudaError_t e;
   if (g.fmt == MOE_FMT_W2) {
     if ((e = set_smem_attr<MOE_FMT_W2>()) != cudaSuccess) return e;
-    gemm_tc_kernel<MOE_FMT_W2><<<grid, kThreads, kSmemBytes, st>>>(a, tmap, tmap_d);
+    gemm_tc_kernel<MOE_FMT_W2><<<grid, kThreads, kSmemBytes, st>>>(a, tmap, tmap_d, tmap_w);
   } else {
     if ((e = set_smem_attr<MOE_FMT_W4NL>()) != cudaSuccess) return e;
-    gemm_tc_kernel<MOE_FMT_W4NL><<<grid, kThreads, kSmemBytes, st>>>(a, tmap, tmap_d);
+    gemm_tc_kernel<MOE_FMT_W4NL><<<grid, kThreads, kSmemBytes, st>>>(a, tmap, tmap_d, tmap_w);
   }
   count_launch();
   return cudaGetLastError();

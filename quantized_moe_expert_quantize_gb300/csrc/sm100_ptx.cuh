@@ -64,16 +64,21 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 // Wait for the phase with the given parity to complete, giving up after
 // `timeout_ns` (or as soon as *abort is set by another thread).  On a
 // timeout the caller's role stops; the kernel then drains and returns.
+// Roles off the critical path park the warp between polls; latency-critical
+// roles (sleep = false) poll without suspending.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint64_t timeout_ns) {
+                                          uint64_t timeout_ns, bool sleep = true) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (;;) {
-    if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > timeout_ns) {
-      *abort = 1;
-      return false;
+  for (uint32_t i = 1;; ++i) {
+    if (sleep ? mbar_try_wait_sleep(bar, parity, 200000u) : mbar_try_wait(bar, parity))
+      return true;
+    if (sleep || (i & 63u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > timeout_ns) {
+        *abort = 1;
+        return false;
+      }
     }
   }
 }
@@ -89,15 +94,23 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
-// Four rows (y0..y3) of a 2-D tensor map at column x, one box (one row
-// high) each, into 4 consecutive box rows at dst.
-__device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, int x, int y0, int y1,
-                                            int y2, int y3, uint64_t* bar) {
+// Retarget the tensor map held in shared memory at `smem_tmap` to a new
+// global base address (one thread).
+__device__ __forceinline__ void tmap_replace_address(void* smem_tmap, const void* gaddr) {
+  asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;" ::"r"(
+                   smem_u32(smem_tmap)),
+               "l"(gaddr)
+               : "memory");
+}
+// Copy a shared-memory tensor map to its global slot and make it visible to
+// the tensor-map proxy (whole warp), then acquire it for use.
+__device__ __forceinline__ void tmap_publish(void* gslot, const void* smem_tmap) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
+      "tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.gpu.sync.aligned"
+      " [%0], [%1], 128;" ::"l"(gslot),
+      "r"(smem_u32(smem_tmap))
       : "memory");
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(gslot) : "memory");
 }
 
 // One box of a 2-D tensor map at (x, y) into dst.
@@ -108,17 +121,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
-}
-
-// Warm L2 with one box of a 2-D tensor map (no shared memory written).
-__device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap),
-               "r"(x), "r"(y)
-               : "memory");
-}
-// Warm L2 with [src, src + bytes); src 16-byte aligned, bytes % 16 == 0.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
