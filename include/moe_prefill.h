@@ -72,7 +72,8 @@ enum {
   MOE_ERR_WORKSPACE = -5,   /* workspace smaller than moe_prefill_workspace_bytes */
   MOE_ERR_DEVICE = -6,      /* no sm_103 device is current                 */
   MOE_ERR_LAUNCH = -7,      /* a CUDA call failed while enqueueing         */
-  MOE_ERR_DEVICE_STATUS = -8 /* moe_read_status found device-side errors   */
+  MOE_ERR_DEVICE_STATUS = -8, /* moe_read_status found device-side errors  */
+  MOE_ERR_SCRATCH = -9       /* too large for moe_route_noalloc's fixed scratch */
 };
 
 /* Device status bits (moe_read_status). */
@@ -206,6 +207,30 @@ int moe_combine(const MoeLayerDesc *desc, const float *topk_w, float *out,
 int moe_read_status(const MoeLayerDesc *desc, void *workspace,
                     size_t workspace_bytes, int32_t *status,
                     moe_stream_t stream);
+
+/* Routing (the same outputs as moe_route) for callers that cannot allocate
+ * device memory -- code that may only use the buffers handed to it, or that
+ * runs where allocation is not allowed.  The pages have no counterpart: this
+ * entry point is an addition of this library.
+ *   topk_ids  device int32 [T x k] (desc: T, E, k; other fields unused)
+ *   counts    device int32 [E]     rows per expert
+ *   offsets   device int32 [E+1]   exclusive prefix sum of counts
+ *   row_src   device int32 [T*k]   routed row -> flat entry t*k+r (the first
+ *                                  offsets[E] entries are written)
+ *   dst_of    device int32 [T*k]   flat entry -> routed row, -1 where the
+ *                                  expert id is outside [0, E)
+ * Its scratch is a fixed 1 MiB array in the library's device memory (held by
+ * every GPU that loads the library until the process exits) instead of a
+ * workspace: ceil(T*k/1024)*E + 4*floor(T*k/128) + 5*E + 71 int32 must fit
+ * in 262144 (T*k = 163840 with E = 512 needs about 89,000), or
+ * MOE_ERR_SCRATCH is returned with nothing enqueued.  The first call on a
+ * device looks the array's device address up (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  All
+ * calls share the array: calls whose work overlaps on the GPU (other streams,
+ * other threads) race.  Nothing is allocated or freed. */
+int moe_route_noalloc(const MoeLayerDesc *desc, const int32_t *topk_ids,
+                      int32_t *counts, int32_t *offsets, int32_t *row_src,
+                      int32_t *dst_of, moe_stream_t stream);
 
 /* MOE_OK when the current CUDA device is an sm_103 part, else MOE_ERR_DEVICE. */
 int moe_check_device(void);

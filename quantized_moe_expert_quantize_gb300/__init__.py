@@ -29,6 +29,7 @@ MOE_ERR_WORKSPACE = -5
 MOE_ERR_DEVICE = -6
 MOE_ERR_LAUNCH = -7
 MOE_ERR_DEVICE_STATUS = -8
+MOE_ERR_SCRATCH = -9
 
 MOE_STATUS_BAD_EXPERT_ID = 1
 MOE_STATUS_BAD_OFFSET = 2
@@ -40,7 +41,7 @@ EXPORTS = (
     "moe_prefill_workspace_bytes", "moe_workspace_view", "moe_prefill_layer",
     "moe_host_io_bytes", "moe_prefill_layer_host", "moe_route", "moe_quant_q8",
     "moe_gate_up", "moe_swiglu_quant", "moe_down", "moe_combine", "moe_read_status",
-    "moe_check_device", "moe_status_string", "moe_kernel_launches",
+    "moe_check_device", "moe_status_string", "moe_kernel_launches", "moe_route_noalloc",
 )
 
 
@@ -104,6 +105,8 @@ def lib(build_if_missing: bool = False) -> ctypes.CDLL:
         L.moe_down.restype = i32
         L.moe_combine.argtypes = [dp, vp, vp, vp, sz, vp]
         L.moe_combine.restype = i32
+        L.moe_route_noalloc.argtypes = [dp, vp, vp, vp, vp, vp, vp]
+        L.moe_route_noalloc.restype = i32
         L.moe_read_status.argtypes = [dp, vp, sz, ctypes.POINTER(ctypes.c_int32), vp]
         L.moe_read_status.restype = i32
         L.moe_check_device.argtypes = []
@@ -217,6 +220,15 @@ def moe_route(desc, topk_ids, workspace, stream=None):
     _check(lib().moe_route(ctypes.byref(desc), _ptr(topk_ids, torch.int32),
                            _ptr(workspace, torch.uint8), workspace.numel(), _stream(stream)),
            "moe_route")
+
+
+def moe_route_noalloc(desc, topk_ids, counts, offsets, row_src, dst_of, stream=None):
+    """Routing into caller buffers with no workspace and no allocation (the
+    library's fixed device scratch is used instead; see the C header)."""
+    _check(lib().moe_route_noalloc(ctypes.byref(desc), _ptr(topk_ids, torch.int32),
+                                   _ptr(counts, torch.int32), _ptr(offsets, torch.int32),
+                                   _ptr(row_src, torch.int32), _ptr(dst_of, torch.int32),
+                                   _stream(stream)), "moe_route_noalloc")
 
 
 def moe_quant_q8(desc, x, workspace, stream=None):

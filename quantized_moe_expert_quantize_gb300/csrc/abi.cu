@@ -364,6 +364,7 @@ const char* moe_status_string(int code) {
     case MOE_ERR_DEVICE: return "no sm_103 device is current";
     case MOE_ERR_LAUNCH: return "a CUDA call failed while enqueueing";
     case MOE_ERR_DEVICE_STATUS: return "device-side status bits were set";
+    case MOE_ERR_SCRATCH: return "too large for the fixed scratch of moe_route_noalloc";
     default: return "unknown status code";
   }
 }

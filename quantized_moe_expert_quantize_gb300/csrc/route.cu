@@ -16,6 +16,8 @@
 //                       time; __match_any_sync groups lanes of equal expert,
 //                       a lane's rank among them keeps flat order, so rows of
 //                       a bucket come out in increasing flat index t*k + r.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -177,4 +179,89 @@ cudaError_t launch_route(const int32_t* ids, int64_t n, int E, int32_t* hist,
   return cudaGetLastError();
 }
 
+
+// ------------------------------------------------------------------------
+// Routing without caller-provided scratch (moe_route_noalloc).
+//
+// Some callers cannot allocate device memory at the point where they route
+// a batch: code running inside another framework's allocator-free region,
+// or a host that only hands over its own input and output buffers.  For
+// them the routing step's scratch (the per-chunk histogram, the expert order
+// and the tile list) lives in this fixed array instead of in a workspace.
+// Every GPU that loads the library keeps it (1 MiB) until the process exits.
+// All calls share it, so calls whose work overlaps on the GPU race.
+namespace {
+
+constexpr int64_t kNoAllocScratchInts = 1 << 18;  // 1 MiB of int32
+static __device__ __align__(256) int32_t g_route_scratch[kNoAllocScratchInts];
+
+// layout in ints: [0] status bits, [1] tile count, [64..] expert order,
+// then the tile list (int4), then the chunk histogram
+struct NoAllocLayout {
+  int64_t order, tiles, hist, total;
+};
+NoAllocLayout noalloc_layout(int64_t n, int E) {
+  NoAllocLayout L;
+  L.order = 64;
+  L.tiles = (L.order + E + 3) & ~(int64_t)3;  // 16-byte aligned
+  L.hist = L.tiles + 4 * max_tiles(n, E);
+  L.total = L.hist + (int64_t)route_chunks(n) * E;
+  return L;
+}
+
+// Device address of the scratch array on the current device, found once per
+// device with that device current.  The host-side name of the array is only
+// a stand-in and must never be handed to a kernel.
+int32_t* noalloc_scratch(int* err) {
+  static std::mutex mu;
+  static int32_t* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *err = MOE_ERR_DEVICE;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) {
+      *err = MOE_ERR_LAUNCH;
+      return nullptr;
+    }
+    addr[dev] = static_cast<int32_t*>(p);
+  }
+  return addr[dev];
+}
+
+}  // namespace
 }  // namespace moe
+
+extern "C" int moe_route_noalloc(const MoeLayerDesc* desc, const int32_t* topk_ids,
+                                 int32_t* counts, int32_t* offsets, int32_t* row_src,
+                                 int32_t* dst_of, moe_stream_t stream) {
+  using namespace moe;
+  if (!desc) return MOE_ERR_NULL;
+  if (desc->T < 0 || desc->E < 1 || desc->E > 1024 || desc->k < 1 || desc->k > desc->E ||
+      (int64_t)desc->T * desc->k >= ((int64_t)1 << 24))
+    return MOE_ERR_SHAPE;
+  const int64_t n = (int64_t)desc->T * desc->k;
+  if (!counts || !offsets || (n > 0 && (!topk_ids || !row_src || !dst_of))) return MOE_ERR_NULL;
+  const NoAllocLayout L = noalloc_layout(n, desc->E);
+  if (L.total > kNoAllocScratchInts) return MOE_ERR_SCRATCH;
+  int major = 0, minor = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      major != 10 || minor != 3)
+    return MOE_ERR_DEVICE;
+  int err = MOE_OK;
+  int32_t* scratch = noalloc_scratch(&err);
+  if (!scratch) return err;
+  cudaStream_t st = (cudaStream_t)stream;
+  // the status word is accumulated with atomics: start it at zero
+  if (cudaMemsetAsync(scratch, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_LAUNCH;
+  const cudaError_t e =
+      launch_route(topk_ids, n, desc->E, scratch + L.hist, counts, offsets, scratch + L.order,
+                   row_src, dst_of, reinterpret_cast<int4*>(scratch + L.tiles), scratch + 1,
+                   scratch, st);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+}

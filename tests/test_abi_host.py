@@ -100,3 +100,15 @@ def test_status_strings(lib):
     for code in range(-8, 1):
         assert M.status_string(code) != "unknown status code"
     assert M.status_string(-99) == "unknown status code"
+
+
+def test_noalloc_route_rejects_sizes_beyond_its_scratch(lib):
+    """The fixed-scratch routing entry point refuses a problem its 1 MiB
+    scratch cannot hold, before touching the device."""
+    d = M.make_desc(1_000_000, 256, 64, 512, 10)
+    fake = ctypes.c_void_p(1 << 40)  # never dereferenced
+    rc = lib.moe_route_noalloc(ctypes.byref(d), fake, fake, fake, fake, fake, None)
+    assert rc == M.MOE_ERR_SCRATCH
+    assert "scratch" in M.status_string(rc)
+    d = M.make_desc(64, 256, 64, 8, 2)
+    assert lib.moe_route_noalloc(ctypes.byref(d), fake, None, fake, fake, fake, None) == M.MOE_ERR_NULL
