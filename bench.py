@@ -200,12 +200,14 @@ def run_ours(args):
     L = synth.config_layer(args.config)
     s = L.shape
     dev = f"cuda:{local}"
-    desc = M.make_desc(s.T, s.d, s.n_ff, s.E, s.k, s.gu_fmt, s.down_fmt, L.weight_pack.size)
     x = torch.from_numpy(L.x).to(dev)
     ids = torch.from_numpy(L.topk_ids).to(dev)
     w = torch.from_numpy(L.topk_w).to(dev)
-    pack = torch.from_numpy(L.weight_pack).to(dev)
-    eoff = torch.from_numpy(L.expert_offsets).to(dev)
+    # weights: uploaded row-major, tiled once (load time, outside every timed region)
+    desc, pack, eoff = M.tile_weights(s.T, s.d, s.n_ff, s.E, s.k, s.gu_fmt, s.down_fmt,
+                                      torch.from_numpy(L.weight_pack).to(dev),
+                                      torch.from_numpy(L.expert_offsets).to(dev))
+    torch.cuda.synchronize()
     out = torch.empty((s.T, s.d), dtype=torch.float32, device=dev)
     ws = M.alloc_workspace(desc, dev)
     stream = torch.cuda.current_stream()

@@ -87,9 +87,7 @@ enum {
 
 /* Supported shapes: T >= 0; d a multiple of 128, 128 <= d <= 8192; n_ff a
  * multiple of 64, 64 <= n_ff <= 4096; 1 <= E <= 1024; 1 <= k <= E;
- * T*k < 2^24.  Each weight matrix's 128-row tile is staged in shared memory:
- * either it fits in 45 KB (K <= 1280 for W2, K <= 640 for W4NL) or its K is a
- * multiple of 512 (W2) / 256 (W4NL).  Other shapes return MOE_ERR_SHAPE. */
+ * T*k < 2^24.  Other shapes return MOE_ERR_SHAPE. */
 typedef struct MoeLayerDesc {
   int32_t T;        /* tokens                                        */
   int32_t d;        /* hidden size (gate/up K, down output rows)      */
@@ -101,7 +99,7 @@ typedef struct MoeLayerDesc {
   int32_t gu_layout;/* MOE_GU_SPLIT                                   */
   uint32_t flags;   /* must be 0                                      */
   int32_t reserved; /* must be 0                                      */
-  int64_t weight_pack_bytes; /* size of weight_pack; expert matrices must lie inside */
+  int64_t weight_pack_bytes; /* size of the tiled weight pack; expert matrices must lie inside */
 } MoeLayerDesc;
 
 /* Device pointers into a workspace, as laid out by this library.  Every
@@ -144,15 +142,52 @@ size_t moe_prefill_workspace_bytes(const MoeLayerDesc *desc);
 int moe_workspace_view(const MoeLayerDesc *desc, void *workspace,
                        size_t workspace_bytes, MoeWorkspaceView *view);
 
+/* Device-tiled weight pack.  The product kernels read the weights in a
+ * tiled byte order, a permutation of the row-major pack made once per layer
+ * (at load time) by moe_tile_weights.  For each weight matrix [N_out x K] of
+ * bpr = K / (values per block) blocks per row:
+ *   tile t covers rows 256t .. 256t+NW-1, NW = min(256, N_out - 256t), and
+ *     starts at byte 256*t*bpr*18 of the matrix;
+ *   chunk c of a tile covers blocks 4c .. 4c+nbc-1, nbc = min(4, bpr - 4c),
+ *     and starts at byte 4*c*NW*18 of the tile;
+ *   inside a chunk, the 16 code bytes (block bytes 2..17) of (tile row r,
+ *     chunk block j) lie at (j*NW + r)*16, then the fp16 scales (block bytes
+ *     0..1) at nbc*NW*16 + (j*NW + r)*2.
+ * A tiled matrix has the row-major matrix's size.  Expert e's gate/up matrix
+ * starts at e*(G + D) and its down matrix at e*(G + D) + G, G and D the
+ * matrices' sizes; moe_tiled_pack_bytes(desc) = E*(G + D). */
+int64_t moe_tiled_pack_bytes(const MoeLayerDesc *desc);
+
+/* Tile a row-major weight pack (the layout of MOE_FMT_W2 / MOE_FMT_W4NL
+ * above: expert e's gate/up matrix [2*n_ff x d] at expert_offsets[2e], its
+ * down matrix [d x n_ff] at expert_offsets[2e+1], each offset a multiple of
+ * 16 and each matrix inside weight_pack_bytes).
+ *   weight_pack    device bytes [weight_pack_bytes], 16-byte aligned
+ *   expert_offsets device int64 [E x 2] (row-major pack offsets)
+ *   tiled_pack     device bytes, 16-byte aligned, desc->weight_pack_bytes of
+ *                  them (>= moe_tiled_pack_bytes(desc), else MOE_ERR_WORKSPACE)
+ *   tiled_offsets  device int64 [E x 2]: written with the tiled pack's offsets
+ *   status         device int32 [1] or NULL: MOE_STATUS_BAD_OFFSET is or-ed
+ *                  in when a source offset is misaligned or runs past
+ *                  weight_pack_bytes (that matrix is written as zeros)
+ * The tiled pack and its offsets are what moe_prefill_layer, moe_gate_up and
+ * moe_down take as weight_pack and expert_offsets. */
+int moe_tile_weights(const MoeLayerDesc *desc, const uint8_t *weight_pack,
+                     int64_t weight_pack_bytes, const int64_t *expert_offsets,
+                     uint8_t *tiled_pack, int64_t *tiled_offsets, int32_t *status,
+                     moe_stream_t stream);
+
 /* The whole layer: route -> q8 -> gate/up -> swiglu_quant -> down -> combine.
  *   x              device fp32 [T x d], row-major
  *   topk_ids       device int32 [T x k], expert of each (token, rank)
  *   topk_w         device fp32 [T x k], combine weight of each (token, rank)
- *   weight_pack    device bytes [weight_pack_bytes], 16-byte aligned
+ *   weight_pack    device bytes [weight_pack_bytes], 16-byte aligned: the
+ *                  tiled pack written by moe_tile_weights
  *   expert_offsets device int64 [E x 2]: byte offsets in weight_pack of expert
- *                  e's gate/up matrix [2*n_ff x d] and down matrix [d x n_ff];
- *                  each must be a multiple of 16 ("a per-layer offset table,
- *                  + the down offset", Strata #3752 commit "moe_ws kernels")
+ *                  e's gate/up matrix [2*n_ff x d] and down matrix [d x n_ff]
+ *                  (the tiled offsets of moe_tile_weights); each must be a
+ *                  multiple of 16 ("a per-layer offset table, + the down
+ *                  offset", Strata #3752 commit "moe_ws kernels")
  *   out            device fp32 [T x d]
  *   workspace      device, 256-byte aligned, >= moe_prefill_workspace_bytes
  * Returns MOE_OK once everything is enqueued on `stream`. */

@@ -42,6 +42,7 @@ EXPORTS = (
     "moe_host_io_bytes", "moe_prefill_layer_host", "moe_route", "moe_quant_q8",
     "moe_gate_up", "moe_swiglu_quant", "moe_down", "moe_combine", "moe_read_status",
     "moe_check_device", "moe_status_string", "moe_kernel_launches", "moe_route_noalloc",
+    "moe_tiled_pack_bytes", "moe_tile_weights",
 )
 
 
@@ -113,6 +114,10 @@ def lib(build_if_missing: bool = False) -> ctypes.CDLL:
         L.moe_check_device.restype = i32
         L.moe_status_string.argtypes = [i32]
         L.moe_status_string.restype = ctypes.c_char_p
+        L.moe_tiled_pack_bytes.argtypes = [dp]
+        L.moe_tiled_pack_bytes.restype = ctypes.c_int64
+        L.moe_tile_weights.argtypes = [dp, vp, ctypes.c_int64, vp, vp, vp, vp, vp]
+        L.moe_tile_weights.restype = i32
         L.moe_kernel_launches.argtypes = []
         L.moe_kernel_launches.restype = ctypes.c_uint64
         _lib = L
@@ -194,6 +199,35 @@ def workspace_view(desc: MoeLayerDesc, ws: torch.Tensor) -> dict:
         nbytes = n * torch.tensor([], dtype=dt).element_size()
         out[name] = ws[off:off + nbytes].view(dt).view(*shape)
     return out
+
+
+def tiled_pack_bytes(desc: MoeLayerDesc) -> int:
+    n = lib().moe_tiled_pack_bytes(ctypes.byref(desc))
+    if n <= 0:
+        raise MoeError(MOE_ERR_SHAPE, "moe_tiled_pack_bytes")
+    return int(n)
+
+
+def moe_tile_weights(desc, weight_pack, expert_offsets, tiled_pack, tiled_offsets, status=None,
+                     stream=None):
+    """Row-major weight pack -> the device-tiled pack the layer reads."""
+    _check(lib().moe_tile_weights(
+        ctypes.byref(desc), _ptr(weight_pack, torch.uint8), weight_pack.numel(),
+        _ptr(expert_offsets, torch.int64), _ptr(tiled_pack, torch.uint8),
+        _ptr(tiled_offsets, torch.int64), _ptr(status, torch.int32), _stream(stream)),
+        "moe_tile_weights")
+
+
+def tile_weights(T, d, n_ff, E, k, gu_fmt, down_fmt, weight_pack, expert_offsets, stream=None):
+    """Tile a device-resident row-major pack; returns (desc, tiled pack,
+    tiled offsets), desc.weight_pack_bytes being the tiled pack's size."""
+    desc = make_desc(T, d, n_ff, E, k, gu_fmt, down_fmt, 0)
+    desc.weight_pack_bytes = tiled_pack_bytes(desc)
+    dev = weight_pack.device
+    tiled = torch.empty(desc.weight_pack_bytes, dtype=torch.uint8, device=dev)
+    toffs = torch.empty((E, 2), dtype=torch.int64, device=dev)
+    moe_tile_weights(desc, weight_pack, expert_offsets, tiled, toffs, None, stream)
+    return desc, tiled, toffs
 
 
 def moe_prefill_layer(desc, x, topk_ids, topk_w, weight_pack, expert_offsets, out, workspace,
@@ -278,14 +312,13 @@ def moe_kernel_launches() -> int:
 
 
 class Layer:
-    """Device-resident weights of one layer plus its workspace, for repeated
-    calls at a fixed token count."""
+    """Device-resident weights of one layer (tiled once, from the row-major
+    pack) plus its workspace, for repeated calls at a fixed token count."""
 
     def __init__(self, T, d, n_ff, E, k, gu_fmt, down_fmt, weight_pack: torch.Tensor,
                  expert_offsets: torch.Tensor, device="cuda"):
-        self.desc = make_desc(T, d, n_ff, E, k, gu_fmt, down_fmt, weight_pack.numel())
-        self.weight_pack = weight_pack
-        self.expert_offsets = expert_offsets
+        self.desc, self.weight_pack, self.expert_offsets = tile_weights(
+            T, d, n_ff, E, k, gu_fmt, down_fmt, weight_pack, expert_offsets)
         self.workspace = alloc_workspace(self.desc, device)
 
     def __call__(self, x, topk_ids, topk_w, out=None, stream=None):

@@ -27,8 +27,7 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t status, counts, offsets, order, tiles, tmaps, row_src, dst_of, hist, xq, dx, gu, hq, dh,
-      dm;
+  size_t status, counts, offsets, order, tiles, row_src, dst_of, hist, xq, dx, gu, hq, dh, dm;
   size_t total;
 };
 
@@ -49,7 +48,6 @@ Layout layout(const MoeLayerDesc& d) {
   L.offsets = take(sizeof(int32_t) * (d.E + 1));
   L.order = take(sizeof(int32_t) * d.E);
   L.tiles = take(sizeof(int4) * (size_t)max_tiles(R, d.E));
-  L.tmaps = take(kTmapSlotBytes);
   L.row_src = take(sizeof(int32_t) * R);
   L.dst_of = take(sizeof(int32_t) * R);
   L.hist = take(sizeof(int32_t) * (size_t)nchunks * d.E);
@@ -75,7 +73,6 @@ int validate_desc(const MoeLayerDesc* d) {
       d->gu_layout != MOE_GU_SPLIT || d->flags != 0 || d->reserved != 0)
     return MOE_ERR_FORMAT;
   if (d->weight_pack_bytes < 0) return MOE_ERR_SHAPE;
-  // the product kernel stages each 128-row weight tile in shared memory
   if (!tc_supported(*d)) return MOE_ERR_SHAPE;
   return MOE_OK;
 }
@@ -145,9 +142,6 @@ int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaSt
   a.which = which;
   a.fmt = which == 0 ? c.d.gu_fmt : c.d.down_fmt;
   a.pack_bytes = c.d.weight_pack_bytes;
-  a.counts = c.v.counts;
-  a.offsets = c.v.offsets;
-  a.order = c.v.order;
   a.tiles = (const int4*)(c.ws + c.L.tiles);
   a.ntiles = c.v.status + 1;
   a.E = c.d.E;
@@ -166,7 +160,7 @@ int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaSt
     a.N_out = c.d.d;
     a.out = c.v.dm;
   }
-  return launch_rc(launch_gemm_tc(a, a.act, c.ws + c.L.tmaps, st));
+  return launch_rc(launch_gemm_tc(a, st));
 }
 
 int run_swiglu(Ctx& c, cudaStream_t st) {
@@ -208,6 +202,28 @@ int moe_workspace_view(const MoeLayerDesc* desc, void* workspace, size_t bytes,
 }
 
 int moe_check_device(void) { return check_device(); }
+
+int64_t moe_tiled_pack_bytes(const MoeLayerDesc* desc) {
+  if (validate_desc(desc)) return 0;
+  return tiled_pack_bytes(*desc);
+}
+
+int moe_tile_weights(const MoeLayerDesc* desc, const uint8_t* weight_pack,
+                     int64_t weight_pack_bytes, const int64_t* expert_offsets,
+                     uint8_t* tiled_pack, int64_t* tiled_offsets, int32_t* status,
+                     moe_stream_t stream) {
+  int rc = validate_desc(desc);
+  if (rc) return rc;
+  if (!weight_pack || !expert_offsets || !tiled_pack || !tiled_offsets) return MOE_ERR_NULL;
+  if (weight_pack_bytes < 0) return MOE_ERR_SHAPE;
+  if (desc->weight_pack_bytes < tiled_pack_bytes(*desc)) return MOE_ERR_WORKSPACE;
+  if (!aligned(weight_pack, 16) || !aligned(tiled_pack, 16) || !aligned(expert_offsets, 8) ||
+      !aligned(tiled_offsets, 8) || !aligned(status, 4))
+    return MOE_ERR_ALIGN;
+  if ((rc = check_device())) return rc;
+  return launch_rc(launch_tile_weights(*desc, weight_pack, weight_pack_bytes, expert_offsets,
+                                       tiled_pack, tiled_offsets, status, (cudaStream_t)stream));
+}
 
 int moe_route(const MoeLayerDesc* desc, const int32_t* topk_ids, void* ws, size_t bytes,
               moe_stream_t stream) {

@@ -65,18 +65,15 @@ cudaError_t launch_combine(const float* topk_w, const int32_t* dst_of, const flo
 
 // ------------------------------------------------------------ products
 struct GemmArgs {
-  const uint8_t* pack;       // weight pack
-  const int64_t* eoff;       // [E][2] byte offsets
+  const uint8_t* pack;       // device-tiled weight pack
+  const int64_t* eoff;       // [E][2] byte offsets in the tiled pack
   int which;                 // 0 = gate/up, 1 = down
   int fmt;                   // MOE_FMT_*
   int64_t pack_bytes;
-  const int32_t* counts;     // [E]
-  const int32_t* offsets;    // [E+1]
-  const int32_t* order;      // [E] largest first
   const int4* tiles;         // routed-row tiles, largest expert first
   const int32_t* ntiles;
   int E;
-  const __half* act;         // activation values (exact fp16 integers)
+  const __half* act;         // activation values [rows_max x K] (exact fp16 integers, routed-row order)
   const float* act_d;        // activation scales [rows_max x scale_stride(K)]
   int K;                     // reduction length
   int N_out;                 // output columns (weight rows)
@@ -84,13 +81,15 @@ struct GemmArgs {
   int64_t rows_max;          // capacity of the routed-row buffers (T*k)
   int32_t* status;
 };
-// tcgen05 product kernel; `act` is the fp16 activation matrix [rows_max x K]
-// in routed-row order
 bool tc_supported(const MoeLayerDesc& d);
-// tmap_slots: global scratch for per-CTA tensor maps, kTmapSlotBytes
-constexpr size_t kTmapSlotBytes = 1024 * 2 * 128;
-cudaError_t launch_gemm_tc(const GemmArgs& a, const void* act, uint8_t* tmap_slots,
-                           cudaStream_t st);
+cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st);
+
+// ------------------------------------------------------- tiled weight pack
+int64_t tiled_matrix_bytes(int fmt, int N_out, int K);
+int64_t tiled_pack_bytes(const MoeLayerDesc& d);
+cudaError_t launch_tile_weights(const MoeLayerDesc& d, const uint8_t* src, int64_t src_bytes,
+                                const int64_t* src_eoff, uint8_t* dst, int64_t* dst_eoff,
+                                int32_t* status, cudaStream_t st);
 
 int device_sm_count();
 

@@ -45,6 +45,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// A poll that never suspends the thread (latency-critical waiters).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // The same with a suspend-time hint: the warp is parked (issuing nothing)
 // until the phase completes or `hint_ns` elapses, so waiting roles do not
 // take issue slots from the roles doing the work.
@@ -65,15 +77,15 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 // `timeout_ns` (or as soon as *abort is set by another thread).  On a
 // timeout the caller's role stops; the kernel then drains and returns.
 // Roles off the critical path park the warp between polls; latency-critical
-// roles (sleep = false) poll without suspending.
+// roles (sleep = false) spin on test_wait, which never suspends.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t timeout_ns, bool sleep = true) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (sleep ? mbar_try_wait_sleep(bar, parity, 200000u) : mbar_try_wait(bar, parity))
+    if (sleep ? mbar_try_wait_sleep(bar, parity, 200000u) : mbar_test_wait(bar, parity))
       return true;
-    if (sleep || (i & 63u) == 0) {
+    if (sleep || (i & 255u) == 0) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > timeout_ns) {
         *abort = 1;
@@ -92,25 +104,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
           "r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
-}
-
-// Retarget the tensor map held in shared memory at `smem_tmap` to a new
-// global base address (one thread).
-__device__ __forceinline__ void tmap_replace_address(void* smem_tmap, const void* gaddr) {
-  asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;" ::"r"(
-                   smem_u32(smem_tmap)),
-               "l"(gaddr)
-               : "memory");
-}
-// Copy a shared-memory tensor map to its global slot and make it visible to
-// the tensor-map proxy (whole warp), then acquire it for use.
-__device__ __forceinline__ void tmap_publish(void* gslot, const void* smem_tmap) {
-  asm volatile(
-      "tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.gpu.sync.aligned"
-      " [%0], [%1], 128;" ::"l"(gslot),
-      "r"(smem_u32(smem_tmap))
-      : "memory");
-  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(gslot) : "memory");
 }
 
 // One box of a 2-D tensor map at (x, y) into dst.
@@ -205,6 +198,20 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t taddr, float2* v) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 16; i++) v[i] = make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+}
+// 32 lanes x 16 consecutive fp32 columns as 8 packed pairs.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t taddr, float2* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; i++) v[i] = make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");

@@ -1,0 +1,112 @@
+// Device-tiled weight pack: a byte permutation of the row-major pack that
+// lets the product kernel stage one (256-row tile, 4-block K chunk) with a
+// single bulk copy and read each block's codes as an aligned 16-byte word.
+//
+// Tiled matrix [N_out x K], bpr = K / values-per-block blocks per row:
+//   tile t covers rows 256t .. 256t+NW-1, NW = min(256, N_out - 256t),
+//     at byte 256 * t * bpr * 18;
+//   chunk c of a tile covers blocks 4c .. 4c+nbc-1, nbc = min(4, bpr - 4c),
+//     at byte 4 * c * NW * 18 of the tile;
+//   inside a chunk: the 16 code bytes of (row r, block j) at (j*NW + r)*16,
+//     then the fp16 scales at nbc*NW*16 + (j*NW + r)*2.
+// Expert e's gate/up matrix starts at e*(gu_bytes + down_bytes), its down
+// matrix gu_bytes later.  Every chunk starts 16-byte aligned.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+struct TileJob {
+  const uint8_t* src;
+  int64_t src_bytes;
+  const int64_t* src_eoff;  // [E][2]
+  uint8_t* dst;
+  int64_t* dst_eoff;        // [E][2]
+  int32_t* status;          // may be null
+  int E;
+  int N[2], K[2], bpr[2];
+  int64_t mbytes[2];        // bytes of one matrix
+};
+
+__global__ void tile_weights_kernel(const TileJob j) {
+  const int e = blockIdx.z >> 1, which = blockIdx.z & 1;
+  const int bpr = j.bpr[which];
+  const int64_t per_expert = j.mbytes[0] + j.mbytes[1];
+  const int64_t dbase = (int64_t)e * per_expert + (which ? j.mbytes[0] : 0);
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+    j.dst_eoff[2 * e + which] = dbase;
+  const int64_t soff = j.src_eoff[2 * e + which];
+  const bool ok = soff >= 0 && (soff & 15) == 0 && soff + j.mbytes[which] <= j.src_bytes;
+  if (!ok && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && j.status)
+    atomicOr(j.status, MOE_STATUS_BAD_OFFSET);
+  // one thread per (row, block)
+  const int64_t n = (int64_t)j.N[which] * bpr;
+  for (int64_t i = (int64_t)blockIdx.y * blockDim.x * gridDim.x + (int64_t)blockIdx.x * blockDim.x +
+                   threadIdx.x;
+       i < n; i += (int64_t)blockDim.x * gridDim.x * gridDim.y) {
+    const int row = (int)(i / bpr), blk = (int)(i % bpr);
+    const int t = row >> 8, r = row & 255;
+    const int nw = min(256, j.N[which] - 256 * t);
+    const int c = blk >> 2, jj = blk & 3, nbc = min(4, bpr - 4 * c);
+    const int64_t chunk = dbase + (int64_t)256 * t * bpr * kBlockBytes +
+                          (int64_t)4 * c * nw * kBlockBytes;
+    uint8_t* codes = j.dst + chunk + ((int64_t)jj * nw + r) * 16;
+    uint16_t* scale = reinterpret_cast<uint16_t*>(j.dst + chunk + (int64_t)nbc * nw * 16 +
+                                                  ((int64_t)jj * nw + r) * 2);
+    uint16_t h[9];
+    if (ok) {
+      const uint16_t* s = reinterpret_cast<const uint16_t*>(
+          j.src + soff + ((int64_t)row * bpr + blk) * kBlockBytes);
+#pragma unroll
+      for (int k = 0; k < 9; k++) h[k] = s[k];
+    } else {
+#pragma unroll
+      for (int k = 0; k < 9; k++) h[k] = 0;
+    }
+    *scale = h[0];
+    *reinterpret_cast<uint4*>(codes) =
+        make_uint4((uint32_t)h[1] | ((uint32_t)h[2] << 16), (uint32_t)h[3] | ((uint32_t)h[4] << 16),
+                   (uint32_t)h[5] | ((uint32_t)h[6] << 16), (uint32_t)h[7] | ((uint32_t)h[8] << 16));
+  }
+}
+
+}  // namespace
+
+int64_t tiled_matrix_bytes(int fmt, int N_out, int K) { return (int64_t)N_out * row_bytes(fmt, K); }
+
+int64_t tiled_pack_bytes(const MoeLayerDesc& d) {
+  return (int64_t)d.E * (tiled_matrix_bytes(d.gu_fmt, 2 * d.n_ff, d.d) +
+                         tiled_matrix_bytes(d.down_fmt, d.d, d.n_ff));
+}
+
+cudaError_t launch_tile_weights(const MoeLayerDesc& d, const uint8_t* src, int64_t src_bytes,
+                                const int64_t* src_eoff, uint8_t* dst, int64_t* dst_eoff,
+                                int32_t* status, cudaStream_t st) {
+  TileJob j{};
+  j.src = src;
+  j.src_bytes = src_bytes;
+  j.src_eoff = src_eoff;
+  j.dst = dst;
+  j.dst_eoff = dst_eoff;
+  j.status = status;
+  j.E = d.E;
+  j.N[0] = 2 * d.n_ff;
+  j.K[0] = d.d;
+  j.N[1] = d.d;
+  j.K[1] = d.n_ff;
+  j.bpr[0] = d.d / block_values(d.gu_fmt);
+  j.bpr[1] = d.n_ff / block_values(d.down_fmt);
+  j.mbytes[0] = tiled_matrix_bytes(d.gu_fmt, j.N[0], j.K[0]);
+  j.mbytes[1] = tiled_matrix_bytes(d.down_fmt, j.N[1], j.K[1]);
+  const int64_t most = std::max((int64_t)j.N[0] * j.bpr[0], (int64_t)j.N[1] * j.bpr[1]);
+  const int threads = 256;
+  const int gx = (int)std::min<int64_t>((most + threads - 1) / threads, 64);
+  dim3 grid(gx, 1, 2 * d.E);
+  tile_weights_kernel<<<grid, threads, 0, st>>>(j);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -66,14 +66,20 @@ class DeviceLayer:
         self.M = M
         self.L = L
         s = L.shape
-        self.desc = M.make_desc(s.T, s.d, s.n_ff, s.E, s.k, s.gu_fmt, s.down_fmt,
-                                L.weight_pack.size)
         dev = "cuda"
         self.x = torch.from_numpy(L.x).to(dev)
         self.ids = torch.from_numpy(L.topk_ids).to(dev)
         self.w = torch.from_numpy(L.topk_w).to(dev)
-        self.pack = torch.from_numpy(L.weight_pack).to(dev)
-        self.eoff = torch.from_numpy(L.expert_offsets).to(dev)
+        # row-major pack as drawn, then the tiled pack the layer reads
+        self.raw_pack = torch.from_numpy(L.weight_pack).to(dev)
+        self.raw_eoff = torch.from_numpy(L.expert_offsets).to(dev)
+        self.desc = M.make_desc(s.T, s.d, s.n_ff, s.E, s.k, s.gu_fmt, s.down_fmt, 0)
+        self.desc.weight_pack_bytes = M.tiled_pack_bytes(self.desc)
+        self.pack = torch.full((self.desc.weight_pack_bytes,), 0xA5, dtype=torch.uint8, device=dev)
+        self.eoff = torch.full((s.E, 2), -1, dtype=torch.int64, device=dev)
+        self.tile_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        M.moe_tile_weights(self.desc, self.raw_pack, self.raw_eoff, self.pack, self.eoff,
+                           self.tile_status)
         self.out = torch.full((max(s.T, 1), s.d), float("nan"), device=dev)[: s.T]
         self.ws = M.alloc_workspace(self.desc)
         self.ws.fill_(0xFF)  # poison: nothing may rely on zeroed workspace

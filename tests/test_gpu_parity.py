@@ -203,14 +203,59 @@ def test_bad_expert_id_is_dropped_and_flagged(M):
 
 
 def test_bad_expert_offset_is_skipped_and_flagged(M):
+    """A row-major offset that is misaligned or runs past the pack is flagged
+    by the tiling step (that matrix becomes zeros); a tiled offset that is
+    misaligned or runs past the tiled pack is flagged by the layer, and that
+    expert is skipped."""
     shape = synth.LayerShape(16, 256, 64, 4, 1)
     L = synth.make_layer(shape, seed=6, routing="topk")
     L.expert_offsets = L.expert_offsets.copy()
     L.expert_offsets[0, 1] = L.weight_pack.size - 8   # runs past the pack
-    L.expert_offsets[1, 0] += 2                       # misaligned
     dl = DeviceLayer(M, L)
+    torch.cuda.synchronize()
+    assert int(dl.tile_status.item()) & M.MOE_STATUS_BAD_OFFSET
+    dl.run_layer()
+    assert dl.status() == 0
+    dl.eoff[1:, 0] += 2                                 # misaligned
+    dl.eoff[2, 1] = dl.desc.weight_pack_bytes - 16      # runs past the tiled pack
     dl.run_layer()
     assert dl.status() & M.MOE_STATUS_BAD_OFFSET
+
+
+def _tile_reference(pack, eoff, fmt_gu, fmt_dn, d, n_ff, E):
+    """The tiled layout of the C header, written out with numpy."""
+    out = []
+    for e in range(E):
+        for which, (fmt, N, K) in enumerate(((fmt_gu, 2 * n_ff, d), (fmt_dn, d, n_ff))):
+            bpr = K // synth.BLOCK_VALUES[fmt]
+            m = pack[eoff[e, which]:eoff[e, which] + N * bpr * 18].reshape(N, bpr, 18)
+            for t in range(0, N, 256):
+                nw = min(256, N - t)
+                for c in range(0, bpr, 4):
+                    blk = m[t:t + nw, c:c + 4]                 # [nw, nbc, 18]
+                    out.append(blk[:, :, 2:].transpose(1, 0, 2).reshape(-1))
+                    out.append(blk[:, :, :2].transpose(1, 0, 2).reshape(-1))
+    return np.concatenate(out)
+
+
+@pytest.mark.parametrize("shape", [synth.LayerShape(8, 384, 192, 3, 2, synth.W2, synth.W4NL),
+                                   synth.LayerShape(8, 640, 320, 2, 1, synth.W4NL, synth.W2)])
+def test_tiled_pack_layout(M, shape):
+    """moe_tile_weights writes exactly the documented byte permutation, with
+    ragged last tiles (N_out % 256 == 128) and ragged last chunks."""
+    L = synth.make_layer(shape, seed=12, routing="topk")
+    dl = DeviceLayer(M, L)
+    torch.cuda.synchronize()
+    assert int(dl.tile_status.item()) == 0
+    ref = _tile_reference(L.weight_pack, L.expert_offsets, shape.gu_fmt, shape.down_fmt,
+                          shape.d, shape.n_ff, shape.E)
+    got = dl.pack.cpu().numpy()
+    assert got.size == ref.size
+    assert np.array_equal(got, ref)
+    gu = 2 * shape.n_ff * synth.row_bytes(shape.gu_fmt, shape.d)
+    dn = shape.d * synth.row_bytes(shape.down_fmt, shape.n_ff)
+    want = np.array([[e * (gu + dn), e * (gu + dn) + gu] for e in range(shape.E)])
+    assert np.array_equal(dl.eoff.cpu().numpy(), want)
 
 
 def test_host_buffers_entry_point(M):
