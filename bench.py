@@ -243,11 +243,11 @@ def run_ours(args):
     value = world * s.T * args.steps / (ms / 1e3)
 
     # ---- per-stage device times (same stream, events between stage calls)
-    stages = ["route", "quant_q8", "gate_up", "swiglu_quant", "down", "combine"]
+    # the layer's own steps (gate/up with swiglu_quant fused, as moe_prefill_layer runs it)
+    stages = ["route", "quant_q8", "gate_up_swiglu", "down", "combine"]
     calls = [lambda: M.moe_route(desc, ids, ws, stream),
              lambda: M.moe_quant_q8(desc, x, ws, stream),
-             lambda: M.moe_gate_up(desc, pack, eoff, ws, stream),
-             lambda: M.moe_swiglu_quant(desc, ws, stream),
+             lambda: M.moe_gate_up_swiglu(desc, pack, eoff, ws, stream),
              lambda: M.moe_down(desc, pack, eoff, ws, stream),
              lambda: M.moe_combine(desc, w, out, ws, stream)]
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
@@ -294,7 +294,7 @@ def run_ours(args):
 
     R = s.T * s.k
     peaks = load_peaks()
-    gu_ms = stage_ms["gate_up"]
+    gu_ms = stage_ms["gate_up_swiglu"]
     gu_flops = 2.0 * R * (2 * s.n_ff) * s.d
     achieved = gu_flops / (gu_ms * 1e-3) / 1e12
     pairs = R * (2 * s.n_ff) * (s.d // 32)
@@ -314,11 +314,11 @@ def run_ours(args):
                          "intermediates > 2.5 GB) through a 129 MB L2"},
         "effective_int8_tops": value * s.k * ops_per_row(s) / 1e12,
         "stage_ms": stage_ms,
-        "roofline": {"bound": "tensor", "kernel": "gate_up", "achieved": achieved,
+        "roofline": {"bound": "tensor", "kernel": "gate_up_swiglu", "achieved": achieved,
                      "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16"],
                      "traffic": None, "peak_source": peaks["source"] + " bf16 dense burst",
                      "algorithmic": f"2*R*2*n_ff*d = {gu_flops:.4g} flop per launch"},
-        "roofline_alu": {"bound": "alu", "kernel": "gate_up", "achieved": alu_achieved,
+        "roofline_alu": {"bound": "alu", "kernel": "gate_up_swiglu", "achieved": alu_achieved,
                          "peak": alu_peak, "unit": "T fp32 lane-ops/s",
                          "frac": alu_achieved / alu_peak,
                          "algorithmic": "2 ops (mul, fma) per (output, 32-value block)"},

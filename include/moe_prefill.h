@@ -146,8 +146,11 @@ int moe_workspace_view(const MoeLayerDesc *desc, void *workspace,
  * tiled byte order, a permutation of the row-major pack made once per layer
  * (at load time) by moe_tile_weights.  For each weight matrix [N_out x K] of
  * bpr = K / (values per block) blocks per row:
- *   tile t covers rows 256t .. 256t+NW-1, NW = min(256, N_out - 256t), and
- *     starts at byte 256*t*bpr*18 of the matrix;
+ *   tile t holds NW = min(256, N_out - 256t) rows and starts at byte
+ *     256*t*bpr*18 of the matrix.  Down: rows 256t .. 256t+NW-1.  Gate/up:
+ *     gate rows 128t .. 128t+NW/2-1, then up rows n_ff+128t ..
+ *     n_ff+128t+NW/2-1 (tile row r < NW/2 is gate row 128t+r, tile row
+ *     NW/2+r is up row n_ff+128t+r);
  *   chunk c of a tile covers blocks 4c .. 4c+nbc-1, nbc = min(4, bpr - 4c),
  *     and starts at byte 4*c*NW*18 of the tile;
  *   inside a chunk, the 16 code bytes (block bytes 2..17) of (tile row r,
@@ -177,7 +180,8 @@ int moe_tile_weights(const MoeLayerDesc *desc, const uint8_t *weight_pack,
                      uint8_t *tiled_pack, int64_t *tiled_offsets, int32_t *status,
                      moe_stream_t stream);
 
-/* The whole layer: route -> q8 -> gate/up -> swiglu_quant -> down -> combine.
+/* The whole layer: route -> q8 -> gate/up with swiglu_quant fused -> down ->
+ * combine (the gu region of the workspace is not written).
  *   x              device fp32 [T x d], row-major
  *   topk_ids       device int32 [T x k], expert of each (token, rank)
  *   topk_w         device fp32 [T x k], combine weight of each (token, rank)
@@ -228,6 +232,12 @@ int moe_quant_q8(const MoeLayerDesc *desc, const float *x, void *workspace,
 int moe_gate_up(const MoeLayerDesc *desc, const uint8_t *weight_pack,
                 const int64_t *expert_offsets, void *workspace,
                 size_t workspace_bytes, moe_stream_t stream);
+/* gate/up with swiglu_quant fused into its epilogue: writes hq and dh (as
+ * moe_gate_up followed by moe_swiglu_quant would, bit for bit) and leaves gu
+ * unwritten.  This is the step moe_prefill_layer runs. */
+int moe_gate_up_swiglu(const MoeLayerDesc *desc, const uint8_t *weight_pack,
+                       const int64_t *expert_offsets, void *workspace,
+                       size_t workspace_bytes, moe_stream_t stream);
 int moe_swiglu_quant(const MoeLayerDesc *desc, void *workspace,
                      size_t workspace_bytes, moe_stream_t stream);
 int moe_down(const MoeLayerDesc *desc, const uint8_t *weight_pack,

@@ -42,7 +42,7 @@ EXPORTS = (
     "moe_host_io_bytes", "moe_prefill_layer_host", "moe_route", "moe_quant_q8",
     "moe_gate_up", "moe_swiglu_quant", "moe_down", "moe_combine", "moe_read_status",
     "moe_check_device", "moe_status_string", "moe_kernel_launches", "moe_route_noalloc",
-    "moe_tiled_pack_bytes", "moe_tile_weights",
+    "moe_tiled_pack_bytes", "moe_tile_weights", "moe_gate_up_swiglu",
 )
 
 
@@ -100,6 +100,8 @@ def lib(build_if_missing: bool = False) -> ctypes.CDLL:
         L.moe_quant_q8.restype = i32
         L.moe_gate_up.argtypes = [dp, vp, vp, vp, sz, vp]
         L.moe_gate_up.restype = i32
+        L.moe_gate_up_swiglu.argtypes = [dp, vp, vp, vp, sz, vp]
+        L.moe_gate_up_swiglu.restype = i32
         L.moe_swiglu_quant.argtypes = [dp, vp, sz, vp]
         L.moe_swiglu_quant.restype = i32
         L.moe_down.argtypes = [dp, vp, vp, vp, sz, vp]
@@ -275,6 +277,13 @@ def moe_gate_up(desc, weight_pack, expert_offsets, workspace, stream=None):
     _check(lib().moe_gate_up(ctypes.byref(desc), _ptr(weight_pack, torch.uint8),
                              _ptr(expert_offsets, torch.int64), _ptr(workspace, torch.uint8),
                              workspace.numel(), _stream(stream)), "moe_gate_up")
+
+
+def moe_gate_up_swiglu(desc, weight_pack, expert_offsets, workspace, stream=None):
+    _check(lib().moe_gate_up_swiglu(ctypes.byref(desc), _ptr(weight_pack, torch.uint8),
+                                    _ptr(expert_offsets, torch.int64),
+                                    _ptr(workspace, torch.uint8), workspace.numel(),
+                                    _stream(stream)), "moe_gate_up_swiglu")
 
 
 def moe_swiglu_quant(desc, workspace, stream=None):

@@ -135,7 +135,8 @@ int run_quant(Ctx& c, const float* x, cudaStream_t st) {
                                   (__half*)c.v.xq, c.v.dx, st));
 }
 
-int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaStream_t st) {
+int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaStream_t st,
+             bool fuse_swiglu = false) {
   GemmArgs a{};
   a.pack = pack;
   a.eoff = eoff;
@@ -153,6 +154,10 @@ int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaSt
     a.K = c.d.d;
     a.N_out = 2 * c.d.n_ff;
     a.out = c.v.gu;
+    if (fuse_swiglu) {
+      a.hq = (__half*)c.v.hq;
+      a.dh = c.v.dh;
+    }
   } else {
     a.act = (const __half*)c.v.hq;
     a.act_d = c.v.dh;
@@ -256,6 +261,16 @@ int moe_gate_up(const MoeLayerDesc* desc, const uint8_t* pack, const int64_t* eo
   return run_gemm(c, 0, pack, eoff, (cudaStream_t)stream);
 }
 
+int moe_gate_up_swiglu(const MoeLayerDesc* desc, const uint8_t* pack, const int64_t* eoff,
+                       void* ws, size_t bytes, moe_stream_t stream) {
+  Ctx c;
+  int rc = open_ctx(desc, ws, bytes, c);
+  if (rc) return rc;
+  if ((rc = check_weights(desc, pack, eoff))) return rc;
+  if ((rc = check_device())) return rc;
+  return run_gemm(c, 0, pack, eoff, (cudaStream_t)stream, true);
+}
+
 int moe_swiglu_quant(const MoeLayerDesc* desc, void* ws, size_t bytes, moe_stream_t stream) {
   Ctx c;
   int rc = open_ctx(desc, ws, bytes, c);
@@ -300,8 +315,7 @@ int moe_prefill_layer(const MoeLayerDesc* desc, const float* x, const int32_t* t
   cudaStream_t st = (cudaStream_t)stream;
   if ((rc = run_route(c, topk_ids, st))) return rc;
   if ((rc = run_quant(c, x, st))) return rc;
-  if ((rc = run_gemm(c, 0, weight_pack, expert_offsets, st))) return rc;
-  if ((rc = run_swiglu(c, st))) return rc;
+  if ((rc = run_gemm(c, 0, weight_pack, expert_offsets, st, true))) return rc;
   if ((rc = run_gemm(c, 1, weight_pack, expert_offsets, st))) return rc;
   return run_combine(c, topk_w, out, st);
 }
@@ -343,8 +357,7 @@ int moe_prefill_layer_host(const MoeLayerDesc* desc, const float* h_x, const int
   }
   if ((rc = run_route(c, d_ids, st))) return rc;
   if ((rc = run_quant(c, d_x, st))) return rc;
-  if ((rc = run_gemm(c, 0, weight_pack, expert_offsets, st))) return rc;
-  if ((rc = run_swiglu(c, st))) return rc;
+  if ((rc = run_gemm(c, 0, weight_pack, expert_offsets, st, true))) return rc;
   if ((rc = run_gemm(c, 1, weight_pack, expert_offsets, st))) return rc;
   if ((rc = run_combine(c, d_w, d_out, st))) return rc;
   if (T > 0 && cudaMemcpyAsync(h_out, d_out, bx, cudaMemcpyDeviceToHost, st) != cudaSuccess)

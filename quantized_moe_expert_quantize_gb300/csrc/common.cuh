@@ -77,7 +77,9 @@ struct GemmArgs {
   const float* act_d;        // activation scales [rows_max x scale_stride(K)]
   int K;                     // reduction length
   int N_out;                 // output columns (weight rows)
-  float* out;                // [rows x N_out]
+  float* out;                // [rows x N_out] (unused when hq is set)
+  __half* hq;                // gate/up only: if set, swiglu_quant is fused and Hq / dh
+  float* dh;                 //   are written instead of GU
   int64_t rows_max;          // capacity of the routed-row buffers (T*k)
   int32_t* status;
 };

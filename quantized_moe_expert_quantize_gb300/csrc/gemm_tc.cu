@@ -41,12 +41,15 @@
 //               store
 //   warps 16-19 weight decode: raw blocks (bulk-copied to shared memory)
 //               -> fp16 operand tile in the 128-byte swizzle layout
-//   warp 20     producer: raw weight chunks of the tiled pack (one bulk copy
-//               per 256-row x 4-block chunk), one 2-D TMA box of the tile's
-//               128 activation rows per stage and one of their scales per
-//               4 blocks
+//   warp 20     producer: one 2-D TMA box of the tile's 128 activation rows
+//               per stage
 //   warp 21     MMA issue (one thread) and TMEM allocation
-//   warps 22-23 idle (the register split needs 24 warps)
+//   warp 22     producer: one 2-D TMA box of the tile's activation scales
+//               per 4 blocks, up to 8 boxes ahead of the epilogue
+//   warp 23     producer: raw weight chunks of the tiled pack (one bulk copy
+//               per 256-row x 4-block chunk), one chunk ahead of the decode
+// Each stream has its own ring and its own warp, so none of them waits
+// behind another's barrier.
 // Activations arrive in routed-row order (the q8 and swiglu_quant steps
 // scatter each row to its routed slot), so a tile's rows are one contiguous
 // range, and pair-interleaved within each 16-value group (position 2i holds
@@ -79,8 +82,10 @@ constexpr int kDwRing = 16;       // W4NL weight scales, one entry per 32-value 
 constexpr int kScaleBox = 4;      // scale columns per TMA box: 16 bytes a row
 constexpr int kEpiWarps = 16;
 constexpr int kWarpDecode = 16;   // warps 16..19
-constexpr int kWarpProducer = 20;
+constexpr int kWarpProducer = 20;  // activations
 constexpr int kWarpMma = 21;
+constexpr int kWarpScales = 22;    // activation scales
+constexpr int kWarpRaw = 23;       // raw weight chunks
 constexpr int kThreads = 768;
 // Register split.  The kernel launches at 80 registers a thread (24 warps);
 // setmaxnreg then moves registers from the other roles to the epilogue.  The
@@ -121,6 +126,10 @@ static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a CTA c
 static_assert(kOffBar % 8 == 0 && kOffEoff % 8 == 0 && kOffRaw % 16 == 0 && kOffDx % 128 == 0,
               "alignment");
 
+// What the epilogue writes: GU rows (gate/up), Hq and its scales (gate/up
+// with swiglu_quant fused), or Dm rows (down).
+constexpr int kModeGU = 0, kModeSwiglu = 1, kModeDown = 2;
+
 struct TcArgs {
   const uint8_t* pack;  // tiled weight pack
   const int64_t* eoff;
@@ -132,7 +141,9 @@ struct TcArgs {
   int K;
   int N_out;
   int bpr;              // weight blocks per row
-  float* out;
+  float* out;           // GU [rows x N_out] or Dm [rows x N_out]
+  __half* hq;           // fused swiglu_quant: Hq [rows x N_out/2], pair-interleaved
+  float* dh;            // fused swiglu_quant: scales [rows x scale_stride(N_out/2)]
   int64_t rows_max;
   int32_t* status;
 };
@@ -235,12 +246,63 @@ __device__ __forceinline__ void decode_w4_store(uint4 codes, const uint16_t* lut
   }
 }
 
+// ------------------------------------------------------------- epilogue
+// 32-byte store of 8 consecutive fp32 values (4 packed pairs); p 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(float* p, const float2* v) {
+  asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(v[0].x),
+               "f"(v[0].y), "f"(v[1].x), "f"(v[1].y), "f"(v[2].x), "f"(v[2].y), "f"(v[3].x),
+               "f"(v[3].y)
+               : "memory");
+}
+__device__ __forceinline__ void st_global_v8_u32(void* p, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+// One q8 block of H from a thread's 32 gate values (acc[0..15]) and the
+// matching 32 up values (acc[16..31]): H = silu(g)*u, each step rounded to
+// fp32 ("Strata #3752", commit "swiglu_quant"), then d = amax/127 and
+// q = rint(h/d) (d = 0 gives q = 0), stored as exact fp16 integers,
+// pair-interleaved in each 16-value group, with the block's scale.
+__device__ __forceinline__ void swiglu_q8_block_store(float2* acc, __half* hq, float* dh) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; j++) {
+    const float2 g = acc[j], u = acc[16 + j];
+    const float h0 = __fmul_rn(__fdiv_rn(g.x, __fadd_rn(1.0f, expf(-g.x))), u.x);
+    const float h1 = __fmul_rn(__fdiv_rn(g.y, __fadd_rn(1.0f, expf(-g.y))), u.y);
+    acc[j] = make_float2(h0, h1);
+    amax = fmaxf(amax, fmaxf(fabsf(h0), fabsf(h1)));
+  }
+  const float d = __fdiv_rn(amax, 127.0f);
+  uint32_t w[16];
+#pragma unroll
+  for (int g = 0; g < 2; g++) {
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      // values 16g+i and 16g+i+8 (acc holds value pairs 2j, 2j+1 in acc[j])
+      const int lo = 16 * g + i, hi = lo + 8;
+      const float vlo = (lo & 1) ? acc[lo >> 1].y : acc[lo >> 1].x;
+      const float vhi = (hi & 1) ? acc[hi >> 1].y : acc[hi >> 1].x;
+      const float q0 = (d == 0.0f) ? 0.0f : rintf(__fdiv_rn(vlo, d));
+      const float q1 = (d == 0.0f) ? 0.0f : rintf(__fdiv_rn(vhi, d));
+      const __half2 hq2 = __floats2half2_rn(q0, q1);  // exact: |q| <= 127
+      w[8 * g + i] = *reinterpret_cast<const uint32_t*>(&hq2);
+    }
+  }
+  st_global_v8_u32(hq, w);
+  st_global_v8_u32(hq + 16, w + 8);
+  *dh = d;
+}
+
 // ---------------------------------------------------------------- kernel
-template <int FMT>
+template <int FMT, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
                const __grid_constant__ CUtensorMap tmap_d) {
   constexpr bool kFold = (FMT == MOE_FMT_W2);
+  constexpr bool kDown = (MODE == kModeDown);
   constexpr int kBps = kFold ? 1 : 2;                  // weight blocks per stage
   constexpr int kSpc = kChunkBlocks / kBps;            // stages per raw chunk
 
@@ -320,7 +382,7 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
     setmaxnreg_inc<Regs<FMT>::epi>();
     const int q = warp & 3, h = warp >> 2;
     const int trow = 32 * q + lane;  // routed row within the tile (TMEM lane)
-    const uint32_t tlane = tmem + ((uint32_t)(32 * q) << 16) + 64 * h;
+    const uint32_t tlane = tmem + ((uint32_t)(32 * q) << 16);
     uint32_t bc = 0, dcnt = 0;
     bool alive = true;
     int4 tnext = load_tile(a, blockIdx.x, total, n_wtiles);
@@ -331,9 +393,18 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
         if (lane == 0 && warp == 0) atomicOr(a.status, MOE_STATUS_BAD_OFFSET);
         continue;
       }
+      // This warp's 64 TMEM columns, 16 per load: down, columns 64h..64h+63
+      // of the tile; gate/up (tile = NWg gate rows, then the matching NWg up
+      // rows), gate columns 32h..32h+31 and the up columns NWg + 32h.. of the
+      // same outputs.
+      const int nwg = I.NW >> 1;
+      int col[4];
+#pragma unroll
+      for (int c = 0; c < 4; c++)
+        col[c] = kDown ? 64 * h + 16 * c : (c < 2 ? 32 * h + 16 * c : nwg + 32 * h + 16 * (c - 2));
       // warp-uniform: this warp's rows and columns hold results
-      const bool active = 32 * q < I.nrows && 64 * h < I.NW;
-      float2 acc[32];  // columns 2i, 2i+1 of this warp's 64
+      const bool active = 32 * q < I.nrows && (kDown ? 64 * h < I.NW : 32 * h < nwg);
+      float2 acc[32];  // columns col[c] + 2j, +1 in acc[8c + j]
 #pragma unroll
       for (int i = 0; i < 32; i++) acc[i] = make_float2(0.0f, 0.0f);
       for (int b = 0; b < nb; b++) {
@@ -349,13 +420,13 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
         if (active) {
           const float dx = sDx[de * (kTM * kScaleBox) + trow * kScaleBox + (b & 3)];
           const float2 dx2 = make_float2(dx, dx);
-          const float* dws = sDw + (gb % kDwRing) * kTN + 64 * h;
+          const float* dws = sDw + (gb % kDwRing) * kTN;
 #pragma unroll
           for (int c = 0; c < 4; c++) {
             // 16 columns per TMEM load; the buffer is handed back once the
             // last load of the block has landed
             float2 v[8];
-            tmem_ld16x2(tlane + buf * kTN + 16 * c, v);
+            tmem_ld16x2(tlane + buf * kTN + col[c], v);
             tmem_wait_ld();
             if (c == 3) {
               tc_fence_before();
@@ -368,7 +439,7 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
             } else {
 #pragma unroll
               for (int j = 0; j < 8; j++) {
-                const float2 w2 = *reinterpret_cast<const float2*>(dws + 16 * c + 2 * j);
+                const float2 w2 = *reinterpret_cast<const float2*>(dws + col[c] + 2 * j);
                 acc[8 * c + j] = __ffma2_rn(__fmul2_rn(w2, dx2), v[j], acc[8 * c + j]);
               }
             }
@@ -379,22 +450,40 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
           if (lane == 0) mbar_arrive(&tempty[buf]);
         }
         // this block's scales are read: release the entries
-        __syncwarp();
-        if (lane == 0) {
-          if ((b & 3) == 3 || b == nb - 1) mbar_arrive(&dempty[de]);
-          if (!kFold) mbar_arrive(&wempty[gb % kDwRing]);
+        if ((b & 3) == 3 || b == nb - 1 || !kFold) {
+          __syncwarp();
+          if (lane == 0) {
+            if ((b & 3) == 3 || b == nb - 1) mbar_arrive(&dempty[de]);
+            if (!kFold) mbar_arrive(&wempty[gb % kDwRing]);
+          }
         }
       }
       if (!alive) break;
       bc += nb;
       dcnt += (nb + 3) / 4;
-      // store: routed row row0 + trow, outputs o0 + 64h .. + 63
-      if (64 * h < I.NW && trow < I.nrows) {
-        float4* outp = reinterpret_cast<float4*>(a.out + (int64_t)(I.row0 + trow) * a.N_out +
-                                                 I.o0 + 64 * h);
+      if (!active || trow >= I.nrows) continue;
+      const int64_t row = I.row0 + trow;  // routed row
+      if (kDown) {
+        // Dm row, outputs o0 + 64h .. + 63: 32-byte stores
+        float* outp = a.out + row * a.N_out + I.o0 + 64 * h;
 #pragma unroll
-        for (int j = 0; j < 16; j++)
-          outp[j] = make_float4(acc[2 * j].x, acc[2 * j].y, acc[2 * j + 1].x, acc[2 * j + 1].y);
+        for (int j = 0; j < 8; j++) st_global_v8(outp + 8 * j, acc + 4 * j);
+      } else if (MODE == kModeGU) {
+        // gate outputs 128t + 32h .. + 31, and the matching up outputs
+        const int o = (I.o0 >> 1) + 32 * h;
+        float* gp = a.out + row * a.N_out + o;
+        float* up = gp + (a.N_out >> 1);
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+          st_global_v8(gp + 8 * j, acc + 4 * j);
+          st_global_v8(up + 8 * j, acc + 16 + 4 * j);
+        }
+      } else {
+        // swiglu_quant fused: H = silu(g) * u for the 32 outputs
+        // o .. o+31 (one q8 block of H), quantized to q8 in registers
+        const int o = (I.o0 >> 1) + 32 * h;
+        swiglu_q8_block_store(acc, a.hq + row * (a.N_out >> 1) + o,
+                              a.dh + row * scale_stride(a.N_out >> 1) + (o >> 5));
       }
     }
   } else if (warp < kWarpDecode + 4) {
@@ -468,62 +557,17 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
       }
     }
   } else if (warp == kWarpProducer) {
-    // ================================================== producer
+    // ================================================== activation producer
     setmaxnreg_dec<Regs<FMT>::other>();
     if (lane == 0) {
       prefetch_tmap(&tmap);
-      prefetch_tmap(&tmap_d);
-      // Raw weight chunks form one stream over this CTA's items, issued one
-      // chunk ahead of the decode (two slots).
-      const int chunks_per_item = (a.bpr + kChunkBlocks - 1) / kChunkBlocks;
-      int64_t r_item = blockIdx.x;
-      int r_chunk = 0;
-      uint32_t issued = 0;
-      Item RI;
-      auto seek_raw = [&]() -> bool {
-        while (r_item < total) {
-          RI = make_item(a, s_eoff, load_tile(a, r_item, total, n_wtiles),
-                         (int)(r_item % n_wtiles));
-          if (RI.ok) return true;
-          r_item += stride;
-        }
-        return false;
-      };
-      bool r_valid = seek_raw();
-      auto issue_raw = [&]() -> bool {
-        if (!r_valid) return true;
-        const uint32_t slot = issued & 1;
-        if (!mbar_wait(&rempty[slot], ((issued >> 1) & 1) ^ 1, s_abort, kTimeoutNs)) return false;
-        const int nbc = min(kChunkBlocks, a.bpr - r_chunk * kChunkBlocks);
-        const uint32_t bytes = (uint32_t)(nbc * RI.NW * kBlockBytes);
-        mbar_arrive_expect_tx(&rfull[slot], bytes);
-        bulk_g2s(sRaw + slot * kRawSlot,
-                 RI.wbase + (int64_t)r_chunk * kChunkBlocks * RI.NW * kBlockBytes, bytes,
-                 &rfull[slot]);
-        issued++;
-        if (++r_chunk == chunks_per_item) {
-          r_chunk = 0;
-          r_item += stride;
-          r_valid = seek_raw();
-        }
-        return true;
-      };
-      bool alive = issue_raw();  // chunk 0
-      uint32_t it = 0, dcnt = 0;
+      uint32_t it = 0;
+      bool alive = true;
       for (int64_t item = blockIdx.x; item < total && alive; item += stride) {
         const Item I = make_item(a, s_eoff, load_tile(a, item, total, n_wtiles),
                                  (int)(item % n_wtiles));
         if (!I.ok) continue;
         for (int s = 0; s < nstages; s++, it++) {
-          if (s % kSpc == 0 && !(alive = issue_raw())) break;  // the next chunk
-          if ((s & 1) == 0) {
-            // scales of blocks 2s .. 2s+3 (the tile's 128 rows)
-            const uint32_t gd = dcnt + (s >> 1), de = gd % kDxRing;
-            if (!(alive = mbar_wait(&dempty[de], ((gd / kDxRing) & 1) ^ 1, s_abort, kTimeoutNs)))
-              break;
-            mbar_arrive_expect_tx(&dfull[de], (uint32_t)kDxBytes);
-            tma_load_2d(sDx + de * (kTM * kScaleBox), &tmap_d, 2 * s, I.row0, &dfull[de]);
-          }
           const int st = it % kStages;
           if (!(alive = mbar_wait(&empty[st], ((it / kStages) & 1) ^ 1, s_abort, kTimeoutNs)))
             break;
@@ -532,7 +576,54 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
           mbar_arrive_expect_tx(&full_tma[st], (uint32_t)kABytes);
           tma_load_2d(sA + st * kABytes, &tmap, s * kSK, I.row0, &full_tma[st]);
         }
-        dcnt += (nb + 3) / 4;
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpScales) {
+    // ================================================== activation-scale producer
+    // runs up to kDxRing entries (4 blocks each) ahead of the epilogue
+    setmaxnreg_dec<Regs<FMT>::other>();
+    if (lane == 0) {
+      prefetch_tmap(&tmap_d);
+      uint32_t gd = 0;
+      bool alive = true;
+      for (int64_t item = blockIdx.x; item < total && alive; item += stride) {
+        const Item I = make_item(a, s_eoff, load_tile(a, item, total, n_wtiles),
+                                 (int)(item % n_wtiles));
+        if (!I.ok) continue;
+        for (int j = 0; j < (nb + 3) / 4; j++, gd++) {
+          // scales of blocks 4j .. 4j+3 of the tile's 128 rows
+          const uint32_t de = gd % kDxRing;
+          if (!(alive = mbar_wait(&dempty[de], ((gd / kDxRing) & 1) ^ 1, s_abort, kTimeoutNs)))
+            break;
+          mbar_arrive_expect_tx(&dfull[de], (uint32_t)kDxBytes);
+          tma_load_2d(sDx + de * (kTM * kScaleBox), &tmap_d, 4 * j, I.row0, &dfull[de]);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpRaw) {
+    // ================================================== raw weight producer
+    // one bulk copy per (256-row tile, 4-block chunk), into two slots
+    setmaxnreg_dec<Regs<FMT>::other>();
+    if (lane == 0) {
+      const int chunks_per_item = (a.bpr + kChunkBlocks - 1) / kChunkBlocks;
+      uint32_t issued = 0;
+      bool alive = true;
+      for (int64_t item = blockIdx.x; item < total && alive; item += stride) {
+        const Item I = make_item(a, s_eoff, load_tile(a, item, total, n_wtiles),
+                                 (int)(item % n_wtiles));
+        if (!I.ok) continue;
+        for (int c = 0; c < chunks_per_item; c++, issued++) {
+          const uint32_t slot = issued & 1;
+          if (!(alive = mbar_wait(&rempty[slot], ((issued >> 1) & 1) ^ 1, s_abort, kTimeoutNs)))
+            break;
+          const int nbc = min(kChunkBlocks, a.bpr - c * kChunkBlocks);
+          const uint32_t bytes = (uint32_t)(nbc * I.NW * kBlockBytes);
+          mbar_arrive_expect_tx(&rfull[slot], bytes);
+          bulk_g2s(sRaw + slot * kRawSlot, I.wbase + (int64_t)c * kChunkBlocks * I.NW * kBlockBytes,
+                   bytes, &rfull[slot]);
+        }
       }
     }
     __syncwarp();
@@ -585,8 +676,6 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
       mbar_wait(fin, 0, s_abort, kTimeoutNs);
     }
     __syncwarp();
-  } else {
-    setmaxnreg_dec<Regs<FMT>::other>();
   }
 
   if (*s_abort && tid == 0) atomicOr(a.status, MOE_STATUS_PIPE_TIMEOUT);
@@ -616,17 +705,17 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 // Shared-memory size attribute, and a check that the kernel was built with
 // the register count the role split assumes (a smaller launch allocation
 // would leave the epilogue's register increase waiting forever).
-template <int FMT>
+template <int FMT, int MODE>
 cudaError_t prepare_kernel() {
   static bool done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
   cudaFuncAttributes attr;
-  cudaError_t e = cudaFuncGetAttributes(&attr, gemm_tc_kernel<FMT>);
+  cudaError_t e = cudaFuncGetAttributes(&attr, gemm_tc_kernel<FMT, MODE>);
   if (e != cudaSuccess) return e;
   if (attr.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
-  e = cudaFuncSetAttribute(gemm_tc_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(gemm_tc_kernel<FMT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
@@ -654,6 +743,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
   a.N_out = g.N_out;
   a.bpr = g.K / block_values(g.fmt);
   a.out = g.out;
+  a.hq = g.hq;
+  a.dh = g.dh;
   a.rows_max = g.rows_max;
   a.status = g.status;
 
@@ -681,14 +772,21 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
   const int64_t tiles_max = max_tiles(g.rows_max, g.E) * (int64_t)((g.N_out + kTN - 1) / kTN);
   const int grid = (int)std::min<int64_t>(std::min<int64_t>(tiles_max, device_sm_count()),
                                           kMaxGrid);
-  cudaError_t e;
+  const int mode = g.which == 1 ? kModeDown : (g.hq ? kModeSwiglu : kModeGU);
+  cudaError_t e = cudaSuccess;
+#define MOE_LAUNCH_TC(F, M)                                                             \
+  if ((e = prepare_kernel<F, M>()) != cudaSuccess) return e;                            \
+  gemm_tc_kernel<F, M><<<grid, kThreads, kSmemBytes, st>>>(a, tmap, tmap_d);
   if (g.fmt == MOE_FMT_W2) {
-    if ((e = prepare_kernel<MOE_FMT_W2>()) != cudaSuccess) return e;
-    gemm_tc_kernel<MOE_FMT_W2><<<grid, kThreads, kSmemBytes, st>>>(a, tmap, tmap_d);
+    if (mode == kModeDown) { MOE_LAUNCH_TC(MOE_FMT_W2, kModeDown) }
+    else if (mode == kModeSwiglu) { MOE_LAUNCH_TC(MOE_FMT_W2, kModeSwiglu) }
+    else { MOE_LAUNCH_TC(MOE_FMT_W2, kModeGU) }
   } else {
-    if ((e = prepare_kernel<MOE_FMT_W4NL>()) != cudaSuccess) return e;
-    gemm_tc_kernel<MOE_FMT_W4NL><<<grid, kThreads, kSmemBytes, st>>>(a, tmap, tmap_d);
+    if (mode == kModeDown) { MOE_LAUNCH_TC(MOE_FMT_W4NL, kModeDown) }
+    else if (mode == kModeSwiglu) { MOE_LAUNCH_TC(MOE_FMT_W4NL, kModeSwiglu) }
+    else { MOE_LAUNCH_TC(MOE_FMT_W4NL, kModeGU) }
   }
+#undef MOE_LAUNCH_TC
   count_launch();
   return cudaGetLastError();
 }

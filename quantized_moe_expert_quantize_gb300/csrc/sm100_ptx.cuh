@@ -80,7 +80,14 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 // roles (sleep = false) spin on test_wait, which never suspends.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t timeout_ns, bool sleep = true) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (sleep) {
+    if (mbar_try_wait(bar, parity)) return true;
+  } else {
+    // short handoffs complete within a few polls: poll before reading the
+    // (slow) global timer that bounds the wait
+    for (int i = 0; i < 64; i++)
+      if (mbar_test_wait(bar, parity)) return true;
+  }
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (sleep ? mbar_try_wait_sleep(bar, parity, 200000u) : mbar_test_wait(bar, parity))

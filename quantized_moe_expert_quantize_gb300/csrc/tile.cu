@@ -3,8 +3,10 @@
 // single bulk copy and read each block's codes as an aligned 16-byte word.
 //
 // Tiled matrix [N_out x K], bpr = K / values-per-block blocks per row:
-//   tile t covers rows 256t .. 256t+NW-1, NW = min(256, N_out - 256t),
-//     at byte 256 * t * bpr * 18;
+//   tile t holds NW = min(256, N_out - 256t) rows, at byte 256 * t * bpr * 18:
+//     down: rows 256t .. 256t+NW-1;
+//     gate/up: gate rows 128t .. 128t+NW/2-1, then the up rows
+//     n_ff+128t .. n_ff+128t+NW/2-1 (a tile yields whole blocks of H);
 //   chunk c of a tile covers blocks 4c .. 4c+nbc-1, nbc = min(4, bpr - 4c),
 //     at byte 4 * c * NW * 18 of the tile;
 //   inside a chunk: the 16 code bytes of (row r, block j) at (j*NW + r)*16,
@@ -47,7 +49,17 @@ __global__ void tile_weights_kernel(const TileJob j) {
                    threadIdx.x;
        i < n; i += (int64_t)blockDim.x * gridDim.x * gridDim.y) {
     const int row = (int)(i / bpr), blk = (int)(i % bpr);
-    const int t = row >> 8, r = row & 255;
+    int t, r;
+    if (which == 1) {
+      t = row >> 8;
+      r = row & 255;
+    } else {
+      // gate/up: tile t pairs gate rows 128t.. with the up rows n_ff + 128t..
+      const int n_ff = j.N[0] >> 1;
+      const int gr = row < n_ff ? row : row - n_ff;
+      t = gr >> 7;
+      r = (gr & 127) + (row < n_ff ? 0 : min(128, n_ff - 128 * t));
+    }
     const int nw = min(256, j.N[which] - 256 * t);
     const int c = blk >> 2, jj = blk & 3, nbc = min(4, bpr - 4 * c);
     const int64_t chunk = dbase + (int64_t)256 * t * bpr * kBlockBytes +

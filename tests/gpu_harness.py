@@ -86,9 +86,11 @@ class DeviceLayer:
         self.v = M.workspace_view(self.desc, self.ws)
 
     def run_layer(self):
+        """The whole layer (gate/up with swiglu_quant fused: gu is not written)."""
         self.M.moe_prefill_layer(self.desc, self.x, self.ids, self.w, self.pack, self.eoff,
                                  self.out, self.ws)
         torch.cuda.synchronize()
+        self.has_gu = False
 
     def run_stages(self):
         M = self.M
@@ -99,6 +101,7 @@ class DeviceLayer:
         M.moe_down(self.desc, self.pack, self.eoff, self.ws)
         M.moe_combine(self.desc, self.w, self.out, self.ws)
         torch.cuda.synchronize()
+        self.has_gu = True
 
     def status(self) -> int:
         return self.M.moe_read_status(self.desc, self.ws)
@@ -163,9 +166,11 @@ def check_full(dl: DeviceLayer, o: dict, report: dict | None = None):
     check_route(dl, o)
     check_q8_x(dl, o)
     R = int(o["offsets"][-1])
-    gu = dl.get("gu", R)
-    r_gu = rel_rms(gu, o["gu"])
-    assert r_gu <= TOL_GU, r_gu
+    r_gu, gu = None, None
+    if dl.has_gu:
+        gu = dl.get("gu", R)
+        r_gu = rel_rms(gu, o["gu"])
+        assert r_gu <= TOL_GU, r_gu
     hq = dl.get("hq", R)
     frac, mx, n = hq_compare(hq, o["hq"])
     assert frac <= TOL_HQ_FRAC and mx <= 1, (frac, mx, n)
@@ -176,7 +181,8 @@ def check_full(dl: DeviceLayer, o: dict, report: dict | None = None):
     r_out = rel_rms(dl.out.cpu().numpy(), o["out"])
     assert r_out <= TOL_OUT, r_out
     if report is not None:
-        report.update(gu_rel_rms=r_gu, gu_exact=bool(np.array_equal(gu, o["gu"])),
+        report.update(gu_rel_rms=r_gu,
+                      gu_exact=None if gu is None else bool(np.array_equal(gu, o["gu"])),
                       hq_diff=n, dh_exact=bool(np.array_equal(dh, o["dh"])), dm_rel_rms=r_dm,
                       out_rel_rms=r_out)
     return dict(gu=r_gu, hq=n, dm=r_dm, out=r_out)

@@ -47,6 +47,22 @@ def test_small_layer_full_parity(M, name, mode):
     check_full(dl, o)
 
 
+@pytest.mark.parametrize("name", ["mid_w2_w2", "mid_w2_w4nl", "mid_w4nl_w4nl", "flat_w2_w4nl"])
+def test_fused_swiglu_equals_stages(M, name):
+    """The layer's gate/up epilogue with swiglu_quant fused writes the same Hq
+    and dh bits as the gate/up stage followed by the swiglu_quant stage."""
+    L = SMALL[name]()
+    dl = DeviceLayer(M, L)
+    dl.run_layer()
+    R = int(dl.get("offsets")[-1])
+    hq_f, dh_f = dl.get("hq", R), dl.get("dh", R)
+    M.moe_gate_up(dl.desc, dl.pack, dl.eoff, dl.ws)
+    M.moe_swiglu_quant(dl.desc, dl.ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(dl.get("hq", R), hq_f)
+    assert np.array_equal(dl.get("dh", R), dh_f)
+
+
 def test_config4_full_parity(M):
     """T=128 full layer (the weight-bandwidth-bound configuration), every
     output against the full oracle."""
@@ -104,8 +120,6 @@ def test_full_size_config_sampled(M, cfg):
     rng = np.random.default_rng(cfg)
     rows = _sample_rows(R, counts, offsets, dl.get("order"), rng)
     gu_o, hq_o, dh_o, dm_o, exp = oracle_rows(L, o, xq, dx, rows)
-    gu_g = dl.v["gu"][torch.from_numpy(rows).cuda()].cpu().numpy()
-    assert rel_rms(gu_g, gu_o) <= TOL_GU
     hq_g = unpair16(dl.v["hq"][torch.from_numpy(rows).cuda()].cpu().numpy())
     dh_g = dl.v["dh"][torch.from_numpy(rows).cuda()][:, : s.n_ff // 32].contiguous().cpu().numpy()
     frac, mx, n = hq_compare(hq_g, hq_o)
@@ -125,6 +139,11 @@ def test_full_size_config_sampled(M, cfg):
     out_g = dl.out[torch.from_numpy(toks).cuda()].cpu().numpy()
     assert rel_rms(out_g, out_ref) <= TOL_OUT
     assert torch.isfinite(dl.out).all()
+    # GU of the sampled rows from the gate/up stage (the layer fuses it away)
+    M.moe_gate_up(dl.desc, dl.pack, dl.eoff, dl.ws)
+    torch.cuda.synchronize()
+    gu_g = dl.v["gu"][torch.from_numpy(rows).cuda()].cpu().numpy()
+    assert rel_rms(gu_g, gu_o) <= TOL_GU
 
 
 # ------------------------------------------------------------- edge cases
@@ -231,8 +250,13 @@ def _tile_reference(pack, eoff, fmt_gu, fmt_dn, d, n_ff, E):
             m = pack[eoff[e, which]:eoff[e, which] + N * bpr * 18].reshape(N, bpr, 18)
             for t in range(0, N, 256):
                 nw = min(256, N - t)
+                if which == 0:   # gate rows t/2 .., then the matching up rows
+                    g0 = t // 2
+                    rows = np.concatenate([m[g0:g0 + nw // 2], m[n_ff + g0:n_ff + g0 + nw // 2]])
+                else:
+                    rows = m[t:t + nw]
                 for c in range(0, bpr, 4):
-                    blk = m[t:t + nw, c:c + 4]                 # [nw, nbc, 18]
+                    blk = rows[:, c:c + 4]                     # [nw, nbc, 18]
                     out.append(blk[:, :, 2:].transpose(1, 0, 2).reshape(-1))
                     out.append(blk[:, :, :2].transpose(1, 0, 2).reshape(-1))
     return np.concatenate(out)
