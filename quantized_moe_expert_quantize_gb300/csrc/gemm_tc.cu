@@ -379,16 +379,19 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
 
   if (warp < kEpiWarps) {
     // ================================================== epilogue
+    // (kept lean in registers: 64 accumulators and 16 loaded values leave
+    // little room, and a spill reload inside the block loop costs more than
+    // recomputing a value)
     setmaxnreg_inc<Regs<FMT>::epi>();
     const int q = warp & 3, h = warp >> 2;
     const int trow = 32 * q + lane;  // routed row within the tile (TMEM lane)
-    const uint32_t tlane = tmem + ((uint32_t)(32 * q) << 16);
-    uint32_t bc = 0, dcnt = 0;
+    const float* dxrow = sDx + trow * kScaleBox;
+    uint32_t gb = 0;  // 32-value blocks consumed so far (TMEM buffer gb & 1)
+    uint32_t gd = 0;  // activation-scale entries consumed so far
     bool alive = true;
-    int4 tnext = load_tile(a, blockIdx.x, total, n_wtiles);
-    for (int64_t item = blockIdx.x; item < total && alive; item += stride) {
-      const Item I = make_item(a, s_eoff, tnext, (int)(item % n_wtiles));
-      tnext = load_tile(a, item + stride, total, n_wtiles);  // prefetch
+    for (int item = blockIdx.x; item < (int)total && alive; item += (int)stride) {
+      const int wtile = item % n_wtiles;
+      const Item I = make_item(a, s_eoff, load_tile(a, item, total, n_wtiles), wtile);
       if (!I.ok) {
         if (lane == 0 && warp == 0) atomicOr(a.status, MOE_STATUS_BAD_OFFSET);
         continue;
@@ -396,21 +399,19 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
       // This warp's 64 TMEM columns, 16 per load: down, columns 64h..64h+63
       // of the tile; gate/up (tile = NWg gate rows, then the matching NWg up
       // rows), gate columns 32h..32h+31 and the up columns NWg + 32h.. of the
-      // same outputs.
+      // same outputs.  tc0 covers loads 0-1, tc1 loads 2-3.
       const int nwg = I.NW >> 1;
-      int col[4];
-#pragma unroll
-      for (int c = 0; c < 4; c++)
-        col[c] = kDown ? 64 * h + 16 * c : (c < 2 ? 32 * h + 16 * c : nwg + 32 * h + 16 * (c - 2));
+      const uint32_t tc0 = tmem + ((uint32_t)(32 * q) << 16) + (kDown ? 64 * h : 32 * h);
+      const uint32_t tc1 = kDown ? tc0 + 32 : tc0 + nwg;
       // warp-uniform: this warp's rows and columns hold results
       const bool active = 32 * q < I.nrows && (kDown ? 64 * h < I.NW : 32 * h < nwg);
-      float2 acc[32];  // columns col[c] + 2j, +1 in acc[8c + j]
+      float2 acc[32];  // columns of load c, pair j in acc[8c + j]
 #pragma unroll
       for (int i = 0; i < 32; i++) acc[i] = make_float2(0.0f, 0.0f);
-      for (int b = 0; b < nb; b++) {
-        const uint32_t gb = bc + b, buf = gb & 1;
-        const uint32_t gd = dcnt + (b >> 2), de = gd % kDxRing;
-        if ((b & 3) == 0 && !(alive = mbar_wait(&dfull[de], (gd / kDxRing) & 1, s_abort, kTimeoutNs, false)))
+      for (int b = 0; b < nb; b++, gb++) {
+        const uint32_t buf = gb & 1, de = gd % kDxRing;
+        if ((b & 3) == 0 &&
+            !(alive = mbar_wait(&dfull[de], (gd / kDxRing) & 1, s_abort, kTimeoutNs, false)))
           break;
         if (!kFold && !(alive = mbar_wait(&wfull[gb % kDwRing], (gb / kDwRing) & 1, s_abort,
                                           kTimeoutNs, false)))
@@ -418,15 +419,15 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
         if (!(alive = mbar_wait(&tfull[buf], (gb >> 1) & 1, s_abort, kTimeoutNs, false))) break;
         tc_fence_after();
         if (active) {
-          const float dx = sDx[de * (kTM * kScaleBox) + trow * kScaleBox + (b & 3)];
+          const float dx = dxrow[de * (kTM * kScaleBox) + (b & 3)];
           const float2 dx2 = make_float2(dx, dx);
-          const float* dws = sDw + (gb % kDwRing) * kTN;
 #pragma unroll
           for (int c = 0; c < 4; c++) {
             // 16 columns per TMEM load; the buffer is handed back once the
             // last load of the block has landed
+            const uint32_t taddr = (c < 2 ? tc0 : tc1) + buf * kTN + 16 * (c & 1);
             float2 v[8];
-            tmem_ld16x2(tlane + buf * kTN + col[c], v);
+            tmem_ld16x2(taddr, v);
             tmem_wait_ld();
             if (c == 3) {
               tc_fence_before();
@@ -437,9 +438,12 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
 #pragma unroll
               for (int j = 0; j < 8; j++) acc[8 * c + j] = __ffma2_rn(dx2, v[j], acc[8 * c + j]);
             } else {
+              // weight scales of the same columns (tile rows)
+              const float* dws = sDw + (gb % kDwRing) * kTN + (taddr & 0xFFFFu) - (buf * kTN) -
+                                 (uint32_t)(tmem & 0xFFFFu);
 #pragma unroll
               for (int j = 0; j < 8; j++) {
-                const float2 w2 = *reinterpret_cast<const float2*>(dws + col[c] + 2 * j);
+                const float2 w2 = *reinterpret_cast<const float2*>(dws + 2 * j);
                 acc[8 * c + j] = __ffma2_rn(__fmul2_rn(w2, dx2), v[j], acc[8 * c + j]);
               }
             }
@@ -450,17 +454,17 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
           if (lane == 0) mbar_arrive(&tempty[buf]);
         }
         // this block's scales are read: release the entries
-        if ((b & 3) == 3 || b == nb - 1 || !kFold) {
+        const bool last_of_entry = (b & 3) == 3 || b == nb - 1;
+        if (last_of_entry || !kFold) {
           __syncwarp();
           if (lane == 0) {
-            if ((b & 3) == 3 || b == nb - 1) mbar_arrive(&dempty[de]);
+            if (last_of_entry) mbar_arrive(&dempty[de]);
             if (!kFold) mbar_arrive(&wempty[gb % kDwRing]);
           }
         }
+        if (last_of_entry) gd++;
       }
       if (!alive) break;
-      bc += nb;
-      dcnt += (nb + 3) / 4;
       if (!active || trow >= I.nrows) continue;
       const int64_t row = I.row0 + trow;  // routed row
       if (kDown) {

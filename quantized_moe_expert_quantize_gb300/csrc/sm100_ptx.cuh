@@ -73,31 +73,33 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete, giving up after
-// `timeout_ns` (or as soon as *abort is set by another thread).  On a
-// timeout the caller's role stops; the kernel then drains and returns.
-// Roles off the critical path park the warp between polls; latency-critical
-// roles (sleep = false) spin on test_wait, which never suspends.
+// Wait for the phase with the given parity to complete; false once the wait
+// gave up (or, for the parked roles, once another thread set *abort).  On a
+// give-up the caller's role stops and *abort is set; the kernel then drains
+// and returns.
+//   sleep = false (the epilogue and the MMA thread): try_wait, which parks
+//     the warp until the phase completes or about 1.4 us pass (measured on
+//     GB300), at most 2^20 times (about 1.4 s).  The bound adds nothing to
+//     the loop but its counter: a periodic abort check or timer in this loop
+//     cost the epilogue ~150 cycles a block in register pressure.
+//   sleep = true (producers, decode): try_wait with a 200 us suspend hint,
+//     bounded by `timeout_ns` of global time, checking *abort between polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t timeout_ns, bool sleep = true) {
-  if (sleep) {
-    if (mbar_try_wait(bar, parity)) return true;
-  } else {
-    // short handoffs complete within a few polls: poll before reading the
-    // (slow) global timer that bounds the wait
-    for (int i = 0; i < 64; i++)
-      if (mbar_test_wait(bar, parity)) return true;
+  if (!sleep) {
+    for (uint32_t i = 0; i < (1u << 20); i++)
+      if (mbar_try_wait(bar, parity)) return true;
+    *abort = 1;
+    return false;
   }
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (sleep ? mbar_try_wait_sleep(bar, parity, 200000u) : mbar_test_wait(bar, parity))
-      return true;
-    if (sleep || (i & 255u) == 0) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > timeout_ns) {
-        *abort = 1;
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      *abort = 1;
+      return false;
     }
   }
 }
