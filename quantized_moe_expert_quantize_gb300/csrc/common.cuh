@@ -46,7 +46,14 @@ inline int route_chunks(int64_t n) { return (int)((n + kRouteChunk - 1) / kRoute
 constexpr int kTileRows = 128;
 __host__ __device__ inline int64_t max_tiles(int64_t rows, int E) { return rows / kTileRows + E + 1; }
 
-// tiles: int4 {expert, first routed row, rows, 0} [max_tiles]; ntiles: int32 [1]
+// Experts with at most kSmallRows routed rows run in the small-expert tier
+// (gemm_small.cu); the rest in the tcgen05 product kernel.
+constexpr int kSmallRows = 16;
+
+// tiles: int4 {expert, first routed row, rows, 0} [max_tiles], largest expert
+// first; ntiles: int32 [2] = {tiles, tiles of experts with more than
+// kSmallRows rows} (those come first, so the small experts' tiles are the
+// tail [ntiles[1], ntiles[0]), one tile each)
 cudaError_t launch_route(const int32_t* ids, int64_t n, int E, int32_t* hist,
                          int32_t* counts, int32_t* offsets, int32_t* order,
                          int32_t* row_src, int32_t* dst_of, int4* tiles, int32_t* ntiles,
@@ -84,7 +91,10 @@ struct GemmArgs {
   int32_t* status;
 };
 bool tc_supported(const MoeLayerDesc& d);
+// tcgen05 kernel: the tiles [0, ntiles[1]) (experts with > kSmallRows rows)
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st);
+// small-expert tier: the tiles [ntiles[1], ntiles[0]) (<= kSmallRows rows each)
+cudaError_t launch_gemm_small(const GemmArgs& a, cudaStream_t st);
 
 // ------------------------------------------------------- tiled weight pack
 int64_t tiled_matrix_bytes(int fmt, int N_out, int K);

@@ -371,7 +371,10 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
   tc_fence_after();
 
   const int n_wtiles = (a.N_out + kTN - 1) / kTN;
-  const int64_t total = (int64_t)max(0, min(*a.ntiles, (int)max_tiles(a.rows_max, a.E))) * n_wtiles;
+  // the big experts' tiles [0, ntiles[1]); the small-expert tier takes the rest
+  const int64_t total =
+      (int64_t)max(0, min(min(a.ntiles[1], a.ntiles[0]), (int)max_tiles(a.rows_max, a.E))) *
+      n_wtiles;
   const int nstages = a.K / kSK;
   const int nb = 2 * nstages;  // 32-value blocks of the reduction
   const uint32_t tmem = *s_tmem;

@@ -83,7 +83,9 @@ route_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E,
   __shared__ int32_t s_cnt[1024];    // rows of expert e
   __shared__ int32_t s_tiles[1024];  // tiles of the expert at rank r
   __shared__ int32_t s_warp[32];
+  __shared__ int32_t s_big;  // tiles of experts with more than kSmallRows rows
   const int tid = threadIdx.x;
+  if (tid == 0) s_big = 0;
   int run = 0;
   if (tid < E) {
     for (int c = 0; c < nchunks; c++) {
@@ -109,12 +111,16 @@ route_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E,
     }
     order[rank] = tid;
     s_tiles[rank] = (run + kTileRows - 1) / kTileRows;
+    if (run > kSmallRows) atomicAdd(&s_big, (run + kTileRows - 1) / kTileRows);
   }
   __syncthreads();
   // first tile of each rank (thread tid stands for rank tid here)
   const int nt = s_tiles[tid];
   const int tbase = block_excl_scan(nt, s_warp);
-  if (tid == 1023) *ntiles = tbase + nt;
+  if (tid == 1023) {
+    ntiles[0] = tbase + nt;
+    ntiles[1] = s_big;  // the big experts' tiles come first (largest first)
+  }
   __syncthreads();
   s_tiles[tid] = tbase;
   __syncthreads();
