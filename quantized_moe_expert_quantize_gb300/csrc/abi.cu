@@ -165,8 +165,8 @@ int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaSt
     a.N_out = c.d.d;
     a.out = c.v.dm;
   }
-  // experts with more than kSmallRows rows on the tcgen05 kernel, the rest on
-  // the small-expert tier (both read the tile list's split point on the device)
+  // 128-row tiles on the tcgen05 kernel, short remainders on the small-row
+  // tier (both read the tile list's split point on the device)
   const cudaError_t e = launch_gemm_tc(a, st);
   if (e != cudaSuccess) return launch_rc(e);
   return launch_rc(launch_gemm_small(a, st));

@@ -41,19 +41,23 @@ constexpr int kRouteChunk = 1024;  // flat entries per warp
 constexpr int kRouteWarps = 8;     // warps per CTA
 inline int route_chunks(int64_t n) { return (int)((n + kRouteChunk - 1) / kRouteChunk); }
 
-// Routed-row tiles of the product kernels: experts in largest-first order,
-// each expert's rows cut into tiles of at most kTileRows rows.
+// Routed-row tiles of the product kernels.  Every expert's rows are cut
+// into tiles of kTileRows rows for the tcgen05 kernel; what is left after
+// its full tiles (rows % kTileRows) goes to the small-row tier in tiles of
+// at most kSmallTileRows rows when it is at most kSmallSplit rows, else it is
+// one more (partial) tcgen05 tile.  A partial tcgen05 tile costs as much as a
+// full one; a small-row tile costs about in proportion to its rows.
 constexpr int kTileRows = 128;
-__host__ __device__ inline int64_t max_tiles(int64_t rows, int E) { return rows / kTileRows + E + 1; }
+constexpr int kSmallTileRows = 32;
+constexpr int kSmallSplit = 32;
+static_assert(kSmallSplit % kSmallTileRows == 0 && kSmallSplit < kTileRows, "split rule");
+__host__ __device__ inline int64_t max_tiles(int64_t rows, int E) {
+  return rows / kTileRows + (int64_t)E * (1 + kSmallSplit / kSmallTileRows) + 1;
+}
 
-// Experts with at most kSmallRows routed rows run in the small-expert tier
-// (gemm_small.cu); the rest in the tcgen05 product kernel.
-constexpr int kSmallRows = 16;
-
-// tiles: int4 {expert, first routed row, rows, 0} [max_tiles], largest expert
-// first; ntiles: int32 [2] = {tiles, tiles of experts with more than
-// kSmallRows rows} (those come first, so the small experts' tiles are the
-// tail [ntiles[1], ntiles[0]), one tile each)
+// tiles: int4 {expert, first routed row, rows, 0} [max_tiles]; ntiles: int32
+// [2] = {all tiles, tcgen05 tiles}.  The tcgen05 tiles come first, experts in
+// largest-first order; the small-row tiles are the tail [ntiles[1], ntiles[0]).
 cudaError_t launch_route(const int32_t* ids, int64_t n, int E, int32_t* hist,
                          int32_t* counts, int32_t* offsets, int32_t* order,
                          int32_t* row_src, int32_t* dst_of, int4* tiles, int32_t* ntiles,
@@ -91,9 +95,9 @@ struct GemmArgs {
   int32_t* status;
 };
 bool tc_supported(const MoeLayerDesc& d);
-// tcgen05 kernel: the tiles [0, ntiles[1]) (experts with > kSmallRows rows)
+// tcgen05 kernel: the tiles [0, ntiles[1])
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st);
-// small-expert tier: the tiles [ntiles[1], ntiles[0]) (<= kSmallRows rows each)
+// small-row tier: the tiles [ntiles[1], ntiles[0]) (<= kSmallTileRows rows each)
 cudaError_t launch_gemm_small(const GemmArgs& a, cudaStream_t st);
 
 // ------------------------------------------------------- tiled weight pack

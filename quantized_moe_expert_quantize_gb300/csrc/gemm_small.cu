@@ -1,5 +1,5 @@
-// Small-expert tier of the grouped expert products: experts with at most
-// kSmallRows (16) routed rows.
+// Small-row tier of the grouped expert products: tiles of at most
+// kSmallTileRows (32) routed rows.
 //
 // Same arithmetic as the tcgen05 kernel -- per 32-value K block the exact
 // integer sum of w_int * q, then the fp32 epilogue in K order ("Strata #3752",
@@ -41,24 +41,33 @@ namespace {
 using namespace ptx;
 
 constexpr int kTN = 256;           // weight rows per item (one tile of the tiled pack)
-constexpr int kWarps = 4;          // compute warps, 64 tile rows each
-constexpr int kThreads = (kWarps + 1) * 32;
-constexpr int kSlots = 4;
+constexpr int kWarps = 8;          // warps, 32 tile rows each (warp 0 also loads the ring)
+constexpr int kThreads = kWarps * 32;
+constexpr int kSlots = 3;
+constexpr int kRows = kSmallTileRows;  // routed rows per small tile (MMA N: up to 4 n8 fragments)
+constexpr int kBoxRows = 16;           // rows per activation box (one or two boxes per tile)
 constexpr int kChunkBlocks = 4;    // weight blocks per chunk of the tiled pack
 constexpr int kChunkVals = 256;    // K values per activation box (a W2 chunk; a W4NL chunk uses 128)
 constexpr int kRawBytes = kChunkBlocks * kTN * kBlockBytes;  // 18,432
-constexpr int kActBytes = kSmallRows * kChunkVals * 2;       // 8,192: 16 rows x 256 fp16
-constexpr int kDxBytes = kSmallRows * (kChunkVals / 32) * 4;  // 512: 16 rows x 8 scales
+constexpr int kActBytes = kRows * kChunkVals * 2;       // 16,384: 32 rows x 256 fp16
+constexpr int kDxBytes = kRows * (kChunkVals / 32) * 4;  // 1,024: 32 rows x 8 scales
 // slots 1024-byte aligned: the activation boxes use the 128-byte swizzle
 constexpr int kSlotBytes = (kRawBytes + kActBytes + kDxBytes + 1023) & ~1023;
 constexpr int kActBox = 64;                                  // values per activation box (128 B)
 constexpr int kOffBar = kSlots * kSlotBytes;
 constexpr int kOffMisc = kOffBar + 2 * kSlots * 8;
-constexpr int kSmemBytes = kOffMisc + 128 + 1024;  // abort flag, W4NL table; + alignment slack
+// misc: abort flag (+0), W4NL table (+64), warp-pair barriers [2][kWarps/2]
+// (+128); then the warp-pair amax exchange [2][kWarps][kRows] fp32
+constexpr int kOffAmax = kOffMisc + 256;
+constexpr int kSmemBytes = kOffAmax + 2 * kWarps * kRows * 4 + 1024;  // + alignment slack
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 constexpr int kModeGU = 0, kModeSwiglu = 1, kModeDown = 2;
 static_assert(kSlotBytes % 1024 == 0 && kRawBytes % 1024 == 0, "swizzled boxes 1024-byte aligned");
-static_assert(kSmemBytes <= 232448 / 2, "two CTAs a multiprocessor");
+static_assert(kRows == 2 * kBoxRows && kRows == 32, "a tile is one or two activation boxes");
+// two CTAs a multiprocessor: 16 warps, 4 per sub-partition, 128 registers each
+static_assert(kSmemBytes + 1024 <= 233472 / 2, "two CTAs a multiprocessor");
+constexpr int kMaxRegs = 65536 / (2 * kThreads);
+static_assert(kMaxRegs == 128, "register cap");
 
 struct SmArgs {
   const uint8_t* pack;
@@ -76,10 +85,23 @@ struct SmArgs {
   int32_t* status;
 };
 
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
+}
+// Four 8x8 b16 matrices from shared memory; lanes 8m..8m+7 give the row
+// addresses of matrix m, and lane (g, cq) receives row g, pair cq of each.
+__device__ __forceinline__ void ldsm_x4(uint32_t saddr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(saddr));
 }
 // D = A(16x16, row) * B(16x8, col) + D, fp16 operands, fp32 accumulate.
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -99,22 +121,19 @@ __device__ __forceinline__ void mma16816c(float (&d)[4], const uint32_t (&a)[4],
         "f"(c[2]), "f"(c[3]));
 }
 
-// W2 fragments without arithmetic.  ws is a code word shifted right by 2*cq
-// (codes of values cq, cq+4, cq+8, cq+12 of the group at bits 0, 8, 16, 24).
-// Pair a: (1024 + c_cq, 1024 + c_{cq+8}); pair b: (1024 + 256 c_{cq+4},
-// 1024 + 256 c_{cq+12}) -- the codes dropped into fp16 mantissas, exact.  The
-// B pairs facing pair b are pre-scaled by 1/256 (exact for |q| <= 127), so
-// every product is an integer: (1024 + c) q on the low half of the group's
-// MMA k and 4q + c q on the high half.  The 1024 / 4 offsets and the code
-// bias 2 are taken out by starting each block's accumulation at
-// -(1026 sum_lo q + 6 sum_hi q), itself one MMA of the constant A below
-// against the same B.  All partial sums are integers below 2^23, so the
-// block sum sum (c-2) q comes out exact.
-__device__ __forceinline__ uint32_t w2_pair_lo(uint32_t ws) { return (ws & 0x00030003u) | 0x64006400u; }
-__device__ __forceinline__ uint32_t w2_pair_hi(uint32_t ws) { return (ws & 0x03000300u) | 0x64006400u; }
+// W2 fragments.  ws is a code word shifted right by 2*cq (codes of values
+// cq, cq+4, cq+8, cq+12 of the group at bits 0, 8, 16, 24).  Pair lo:
+// (c_cq - 2, c_{cq+8} - 2); pair hi: 256 * (c_{cq+4} - 2, c_{cq+12} - 2) --
+// the codes dropped into the mantissas of 1024 (one logic op) and the offset
+// subtracted, exact.  The B pairs facing pair hi are pre-scaled by 1/256
+// (exact for |q| <= 127), so every product is the integer (c - 2) * q.
+__device__ __forceinline__ uint32_t w2_pair_lo(uint32_t ws) {
+  return hsub2_u32((ws & 0x00030003u) | 0x64006400u, 0x64026402u);  // (1024 + c) - 1026
+}
+__device__ __forceinline__ uint32_t w2_pair_hi(uint32_t ws) {
+  return hsub2_u32((ws & 0x03000300u) | 0x64006400u, 0x66006600u);  // (1024 + 256c) - 1536
+}
 constexpr uint32_t kHalfInv256 = 0x1C001C00u;  // fp16 pair (1/256, 1/256)
-constexpr uint32_t kCorrLo = 0xE402E402u;      // fp16 pair (-1026, -1026)
-constexpr uint32_t kCorrHi = 0xE600E600u;      // fp16 pair (-1536, -1536) = -6 * 256
 // W4NL: the fp16 pair (T[idx_i], T[idx_{i+8}]) from the group's two words.
 __device__ __forceinline__ uint32_t w4_pair(uint32_t wlo, uint32_t whi, int i,
                                             const uint16_t* lut) {
@@ -123,20 +142,20 @@ __device__ __forceinline__ uint32_t w4_pair(uint32_t wlo, uint32_t whi, int i,
 
 // One item's products: every chunk of the item's weight tile against its
 // (up to 8 * NNT) routed rows, accumulated per 32-value block in K order into
-// acc (fragment mt of tile rows rbase[mt]..+15, n8 fragment nt).  Tile rows
-// past the tile's end compute garbage from in-slot bytes and are never stored.
-template <int FMT, int NNT>
+// acc (m16 fragment mt = tile rows rbase[mt]..+15, n8 fragment nt).  Tile
+// rows past the tile's end compute garbage from in-slot bytes and are never
+// stored.
+template <int FMT, int NNT, typename Refill>
 __device__ __forceinline__ bool consume_item(const uint8_t* smem, uint64_t* full, uint64_t* empty,
                                              volatile int* s_abort, uint32_t& cc, int nchunks,
-                                             int bpr, int nw, const int (&rbase)[4],
+                                             int bpr, int nw, const int (&rbase)[2],
                                              const uint16_t* s_lut, int lane,
-                                             float (&acc)[4][2][4]) {
+                                             float (&acc)[2][4][4], Refill&& refill) {
   constexpr bool kW2 = (FMT == MOE_FMT_W2);
   constexpr int kBv = kW2 ? 64 : 32;        // values per weight block
   constexpr int kVals = kChunkBlocks * kBv;  // K values per chunk
   constexpr int kQpb = kBv / 32;             // q8 blocks per weight block
   const int g = lane >> 2, cq = lane & 3;
-  const uint32_t ca[4] = {kCorrLo, kCorrLo, kCorrHi, kCorrHi};
   const float zero[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   for (int c = 0; c < nchunks; c++, cc++) {
     const uint32_t slot = cc % kSlots;
@@ -144,105 +163,74 @@ __device__ __forceinline__ bool consume_item(const uint8_t* smem, uint64_t* full
     const uint8_t* sp = smem + slot * kSlotBytes;
     const int nbc = min(kChunkBlocks, bpr - c * kChunkBlocks);
     const uint16_t* scl = reinterpret_cast<const uint16_t*>(sp + nbc * nw * 16);
-    const uint8_t* act = sp + kRawBytes;  // [box][16 rows][128 B], 128-byte swizzle
+    const uint8_t* act = sp + kRawBytes;  // [box][32 rows][128 B], 128-byte swizzle
     const float* dxs = reinterpret_cast<const float*>(sp + kRawBytes + kActBytes);
+#pragma unroll 1
+    for (int j = 0; j < nbc; j++) {
+      float dw[2][2];  // scale of weight block j, tile rows rbase+g / +8
 #pragma unroll
-    for (int j = 0; j < kChunkBlocks; j++) {
-      if (j >= nbc) break;
-      float dw[4][2];   // scale of weight block j, tile rows rbase+g / +8
-#pragma unroll
-      for (int mt = 0; mt < 4; mt++)
+      for (int mt = 0; mt < 2; mt++)
 #pragma unroll
         for (int h = 0; h < 2; h++)
           dw[mt][h] = __half2float(__ushort_as_half(scl[j * nw + rbase[mt] + g + 8 * h]));
 #pragma unroll
       for (int qq = 0; qq < kQpb; qq++) {
         const int qb = j * kQpb + qq;  // q8 block within the chunk
-        // the block's code words for this q8 block (two 16-value groups), rows
-        // rbase+g / +8: W2 words 2qq, 2qq+1; W4NL all four
-        uint2 cw[4][2][2 / kQpb];
+        // B fragments, one ldmatrix.x4 per n8 fragment: matrix 2ks + hf is
+        // routed rows 8nt..8nt+7 at stored positions 8hf..8hf+7 of group
+        // 2qb + ks (16-byte chunk 2*((2qb+ks)%4) + hf of box qb/2, 128-byte
+        // swizzle), so lane (g, cq) receives b[ks][nt][hf]
+        uint32_t b[2][NNT][2];
+        float dx[NNT][2];  // activation scales of routed rows 8nt + 2cq, +1
+        const int lm = lane >> 3, lr = lane & 7;  // this lane's matrix and row
+        const uint32_t bsrc = smem_u32(act + (qb >> 1) * (kRows * kActBox * 2) + lr * 128 +
+                                       (((2 * ((2 * qb + (lm >> 1)) & 3) + (lm & 1)) ^ lr) << 4));
 #pragma unroll
-        for (int mt = 0; mt < 4; mt++)
+        for (int nt = 0; nt < NNT; nt++) {
+          ldsm_x4(bsrc + nt * 8 * 128, b[0][nt][0], b[0][nt][1], b[1][nt][0], b[1][nt][1]);
+          if (kW2) {
+            b[0][nt][1] = hmul2_u32(b[0][nt][1], kHalfInv256);
+            b[1][nt][1] = hmul2_u32(b[1][nt][1], kHalfInv256);
+          }
+          dx[nt][0] = dxs[(8 * nt + 2 * cq) * (kVals / 32) + qb];
+          dx[nt][1] = dxs[(8 * nt + 2 * cq + 1) * (kVals / 32) + qb];
+        }
+#pragma unroll
+        for (int mt = 0; mt < 2; mt++) {
+          // A fragments of both 16-value groups of the block
+          uint32_t af[2][4];
 #pragma unroll
           for (int h = 0; h < 2; h++) {
-            const uint2* src =
-                reinterpret_cast<const uint2*>(sp + (j * nw + rbase[mt] + g + 8 * h) * 16);
-#pragma unroll
-            for (int e = 0; e < 2 / kQpb; e++) cw[mt][h][e] = src[qq + e];
+            const uint8_t* wrow = sp + (j * nw + rbase[mt] + g + 8 * h) * 16;
+            if (kW2) {
+              // code words of groups 2qq, 2qq+1 of the block
+              const uint2 w = *reinterpret_cast<const uint2*>(wrow + 8 * qq);
+              const uint32_t ws0 = w.x >> (2 * cq), ws1 = w.y >> (2 * cq);
+              af[0][h] = w2_pair_lo(ws0);
+              af[0][2 + h] = w2_pair_hi(ws0);
+              af[1][h] = w2_pair_lo(ws1);
+              af[1][2 + h] = w2_pair_hi(ws1);
+            } else {
+              const uint4 w = *reinterpret_cast<const uint4*>(wrow);
+              af[0][h] = w4_pair(w.x, w.y, cq, s_lut);
+              af[0][2 + h] = w4_pair(w.x, w.y, cq + 4, s_lut);
+              af[1][h] = w4_pair(w.z, w.w, cq, s_lut);
+              af[1][2 + h] = w4_pair(w.z, w.w, cq + 4, s_lut);
+            }
           }
-        // B fragments: routed row n = 8nt + g, stored positions 2cq,+1 (16-byte
-        // chunk 2*(grp%4)) and 2cq+8,+9 (chunk 2*(grp%4)+1) of box grp/4
-        uint32_t b[2][NNT][2];
-#pragma unroll
-        for (int ks = 0; ks < 2; ks++) {
-          const int grp = 2 * qb + ks;
-          const uint8_t* box = act + (grp >> 2) * (kSmallRows * kActBox * 2);
 #pragma unroll
           for (int nt = 0; nt < NNT; nt++) {
-            const int n = 8 * nt + g;
-            const uint8_t* row = box + n * 128;
-            const int ch = 2 * (grp & 3);
-            b[ks][nt][0] = *reinterpret_cast<const uint32_t*>(row + ((ch ^ (n & 7)) << 4) + 4 * cq);
-            b[ks][nt][1] =
-                *reinterpret_cast<const uint32_t*>(row + (((ch + 1) ^ (n & 7)) << 4) + 4 * cq);
-            if (kW2) b[ks][nt][1] = hmul2_u32(b[ks][nt][1], kHalfInv256);
-          }
-        }
-        float ci[NNT][4];  // accumulation start of the block
-#pragma unroll
-        for (int nt = 0; nt < NNT; nt++) {
-          if (kW2) {
-            mma16816c(ci[nt], ca, b[0][nt][0], b[0][nt][1], zero);
-            mma16816(ci[nt], ca, b[1][nt][0], b[1][nt][1]);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 4; i++) ci[nt][i] = 0.0f;
-          }
-        }
-        float p[4][NNT][4];  // the block's integer sums
-#pragma unroll
-        for (int ks = 0; ks < 2; ks++) {
-#pragma unroll
-          for (int mt = 0; mt < 4; mt++) {
-            uint32_t af[4];
-#pragma unroll
-            for (int h = 0; h < 2; h++) {
-              if (kW2) {
-                // code word of group 2qq + ks of the block
-                const uint32_t w = ks ? cw[mt][h][0].y : cw[mt][h][0].x;
-                const uint32_t ws = w >> (2 * cq);
-                af[h] = w2_pair_lo(ws);
-                af[2 + h] = w2_pair_hi(ws);
-              } else {
-                const uint2 q2 = cw[mt][h][ks];
-                const uint32_t wlo = q2.x, whi = q2.y;
-                af[h] = w4_pair(wlo, whi, cq, s_lut);
-                af[2 + h] = w4_pair(wlo, whi, cq + 4, s_lut);
-              }
-            }
-#pragma unroll
-            for (int nt = 0; nt < NNT; nt++) {
-              if (ks == 0)
-                mma16816c(p[mt][nt], af, b[0][nt][0], b[0][nt][1], ci[nt]);
-              else
-                mma16816(p[mt][nt], af, b[1][nt][0], b[1][nt][1]);
-            }
-          }
-        }
-        // epilogue of the block, in K order: acc += d_x * (d_w * isum) (W2,
-        // d_w * isum exact) or acc += (d_w * d_x) * isum (W4NL)
-#pragma unroll
-        for (int nt = 0; nt < NNT; nt++) {
-          const float dx0 = dxs[(8 * nt + 2 * cq) * (kVals / 32) + qb];
-          const float dx1 = dxs[(8 * nt + 2 * cq + 1) * (kVals / 32) + qb];
-#pragma unroll
-          for (int mt = 0; mt < 4; mt++) {
+            float p[4];  // the block's integer sums
+            mma16816c(p, af[0], b[0][nt][0], b[0][nt][1], zero);
+            mma16816(p, af[1], b[1][nt][0], b[1][nt][1]);
+            // epilogue of the block, in K order: acc += d_x * (d_w * isum)
+            // (W2, d_w * isum exact) or acc += (d_w * d_x) * isum (W4NL)
 #pragma unroll
             for (int i = 0; i < 4; i++) {
-              const float dx = (i & 1) ? dx1 : dx0;
+              const float dxi = dx[nt][i & 1];
               const float dwr = dw[mt][i >> 1];
-              acc[mt][nt][i] = kW2 ? __fmaf_rn(dx, __fmul_rn(dwr, p[mt][nt][i]), acc[mt][nt][i])
-                                   : __fmaf_rn(__fmul_rn(dwr, dx), p[mt][nt][i], acc[mt][nt][i]);
+              acc[mt][nt][i] = kW2 ? __fmaf_rn(dxi, __fmul_rn(dwr, p[i]), acc[mt][nt][i])
+                                   : __fmaf_rn(__fmul_rn(dwr, dxi), p[i], acc[mt][nt][i]);
             }
           }
         }
@@ -250,26 +238,99 @@ __device__ __forceinline__ bool consume_item(const uint8_t* smem, uint64_t* full
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
+    refill(cc);
   }
   return true;
 }
 
+// One item (small-row tile x 256-row weight tile) of the work list, checked.
+struct ItemInfo {
+  int4 t;        // {expert, first routed row, rows, -}
+  int wt, nw;    // weight tile, its rows
+  int64_t off;   // byte offset of the expert's matrix in the tiled pack
+  bool ok;
+};
+__device__ __forceinline__ ItemInfo item_info(const SmArgs& a, int first, int n_wtiles,
+                                              int64_t mbytes, int item) {
+  ItemInfo I;
+  I.t = __ldg(a.tiles + first + item / n_wtiles);
+  I.wt = item % n_wtiles;
+  I.nw = min(kTN, a.N_out - I.wt * kTN);
+  const bool rows_ok = (unsigned)I.t.x < (unsigned)a.E && I.t.y >= 0 && I.t.z > 0 &&
+                       I.t.z <= kRows && (int64_t)I.t.y + I.t.z <= a.rows_max;
+  I.off = rows_ok ? __ldg(a.eoff + 2 * I.t.x + a.which) : -1;
+  I.ok = rows_ok && I.off >= 0 && (I.off & 15) == 0 && I.off + mbytes <= a.pack_bytes;
+  return I;
+}
+
+// The load side of the ring (lane 0 of warp 0): the next (item, chunk) to
+// load, in the order the warps consume them.  Per chunk: one bulk copy of
+// the raw weight chunk and the tile's activation rows and scales in 2-D TMA
+// boxes of 16 rows (rows past the tile land in rows that are never read).
+struct Producer {
+  int item, c;  // next item (>= total: nothing left) and chunk
+  const uint8_t* wbase;
+  int row0, nw, nbox;
+  uint32_t issued;
+};
+__device__ __forceinline__ void prod_seek(Producer& p, const SmArgs& a, int first, int total,
+                                          int n_wtiles, int64_t mbytes) {
+  for (; p.item < total; p.item += gridDim.x) {
+    const ItemInfo I = item_info(a, first, n_wtiles, mbytes, p.item);
+    if (!I.ok) continue;
+    p.c = 0;
+    p.row0 = I.t.y;
+    p.nw = I.nw;
+    p.nbox = I.t.z > kBoxRows ? 2 : 1;
+    p.wbase = a.pack + I.off + (int64_t)I.wt * kTN * a.bpr * kBlockBytes;
+    return;
+  }
+}
+template <int FMT>
+__device__ __forceinline__ void prod_issue(Producer& p, uint8_t* smem, uint64_t* full,
+                                           const SmArgs& a, const CUtensorMap* tmap,
+                                           const CUtensorMap* tmap_d, int first, int total,
+                                           int n_wtiles, int64_t mbytes, int nchunks) {
+  constexpr int kVals = kChunkBlocks * (FMT == MOE_FMT_W2 ? 64 : 32);
+  const uint32_t slot = p.issued % kSlots;
+  uint8_t* sp = smem + slot * kSlotBytes;
+  const int nbc = min(kChunkBlocks, a.bpr - p.c * kChunkBlocks);
+  const uint32_t raw = (uint32_t)(nbc * p.nw * kBlockBytes);
+  mbar_arrive_expect_tx(&full[slot], raw + (uint32_t)(p.nbox * kBoxRows * kVals * 2) +
+                                         (uint32_t)(p.nbox * kBoxRows * (kVals / 32) * 4));
+  bulk_g2s(sp, p.wbase + (int64_t)p.c * kChunkBlocks * p.nw * kBlockBytes, raw, &full[slot]);
+  for (int hb = 0; hb < p.nbox; hb++) {
+#pragma unroll
+    for (int bx = 0; bx < kVals / kActBox; bx++)
+      tma_load_2d(sp + kRawBytes + bx * (kRows * kActBox * 2) + hb * (kBoxRows * 128), tmap,
+                  p.c * kVals + bx * kActBox, p.row0 + kBoxRows * hb, &full[slot]);
+    tma_load_2d(sp + kRawBytes + kActBytes + hb * (kBoxRows * (kVals / 32) * 4), tmap_d,
+                p.c * (kVals / 32), p.row0 + kBoxRows * hb, &full[slot]);
+  }
+  p.issued++;
+  if (++p.c == nchunks) {
+    p.item += gridDim.x;
+    prod_seek(p, a, first, total, n_wtiles, mbytes);
+  }
+}
+
 template <int FMT, int MODE>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 2)
 gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
                   const __grid_constant__ CUtensorMap tmap_d) {
   constexpr bool kW2 = (FMT == MOE_FMT_W2);
   constexpr bool kDown = (MODE == kModeDown);
-  constexpr int kBv = kW2 ? 64 : 32;                  // values per weight block
-  constexpr int kVals = kChunkBlocks * kBv;           // K values per chunk
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  // 1024-byte aligned base, offset from the shared array itself (an integer
+  // round trip would hide the shared address space from the compiler)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* empty = full + kSlots;
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc);
   uint16_t* s_lut = reinterpret_cast<uint16_t*>(smem + kOffMisc + 64);
+  uint64_t* pairbar = reinterpret_cast<uint64_t*>(smem + kOffMisc + 128);
+  float* s_amax = reinterpret_cast<float*>(smem + kOffAmax);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -277,6 +338,7 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kWarps);
     }
+    for (int i = 0; i < kWarps; i++) mbar_init(&pairbar[i], 64);  // both warps of a pair
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -290,161 +352,160 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
   const int nchunks = (a.bpr + kChunkBlocks - 1) / kChunkBlocks;
   const int64_t mbytes = (int64_t)a.N_out * a.bpr * kBlockBytes;
 
-  if (warp == kWarps) {
-    // ================================================== producer
-    if (lane == 0) {
-      prefetch_tmap(&tmap);
-      prefetch_tmap(&tmap_d);
-      uint32_t cc = 0;
-      bool alive = true;
-      for (int item = blockIdx.x; item < total && alive; item += gridDim.x) {
-        const int4 t = __ldg(a.tiles + first + item / n_wtiles);
-        const int wt = item % n_wtiles;
-        const int nw = min(kTN, a.N_out - wt * kTN);
-        const bool rows_ok = (unsigned)t.x < (unsigned)a.E && t.y >= 0 && t.z > 0 &&
-                             t.z <= kSmallRows && (int64_t)t.y + t.z <= a.rows_max;
-        const int64_t off = rows_ok ? __ldg(a.eoff + 2 * t.x + a.which) : -1;
-        if (!(rows_ok && off >= 0 && (off & 15) == 0 && off + mbytes <= a.pack_bytes)) continue;
-        const uint8_t* wbase = a.pack + off + (int64_t)wt * kTN * a.bpr * kBlockBytes;
-        for (int c = 0; c < nchunks; c++, cc++) {
-          const uint32_t slot = cc % kSlots;
-          if (!(alive = mbar_wait(&empty[slot], ((cc / kSlots) & 1) ^ 1, s_abort, kTimeoutNs)))
-            break;
-          uint8_t* sp = smem + slot * kSlotBytes;
-          const int nbc = min(kChunkBlocks, a.bpr - c * kChunkBlocks);
-          const uint32_t raw = (uint32_t)(nbc * nw * kBlockBytes);
-          mbar_arrive_expect_tx(&full[slot], raw + (uint32_t)(kSmallRows * kVals * 2) +
-                                                 (uint32_t)(kSmallRows * (kVals / 32) * 4));
-          bulk_g2s(sp, wbase + (int64_t)c * kChunkBlocks * nw * kBlockBytes, raw, &full[slot]);
-          // the expert's (up to 16) activation rows and their scales; rows
-          // past the expert land in rows that are never read
-#pragma unroll
-          for (int bx = 0; bx < kVals / kActBox; bx++)
-            tma_load_2d(sp + kRawBytes + bx * (kSmallRows * kActBox * 2), &tmap,
-                        c * kVals + bx * kActBox, t.y, &full[slot]);
-          tma_load_2d(sp + kRawBytes + kActBytes, &tmap_d, c * (kVals / 32), t.y, &full[slot]);
-        }
+  // ring: prefill every slot, then lane 0 of warp 0 refills a slot as soon
+  // as all warps have released it
+  Producer prod;
+  prod.item = blockIdx.x;
+  prod.issued = 0;
+  if (tid == 0) {
+    prefetch_tmap(&tmap);
+    prefetch_tmap(&tmap_d);
+    prod_seek(prod, a, first, total, n_wtiles, mbytes);
+    for (int s = 0; s < kSlots && prod.item < total; s++)
+      prod_issue<FMT>(prod, smem, full, a, &tmap, &tmap_d, first, total, n_wtiles, mbytes, nchunks);
+  }
+  auto refill = [&](uint32_t done) {  // chunk `done` was consumed by this warp
+    if (warp == 0) {
+      if (lane == 0 && prod.item < total) {
+        // all warps released chunk `done`'s slot: load the chunk kSlots ahead
+        if (mbar_wait(&empty[done % kSlots], (done / kSlots) & 1, s_abort, kTimeoutNs, false))
+          prod_issue<FMT>(prod, smem, full, a, &tmap, &tmap_d, first, total, n_wtiles, mbytes,
+                          nchunks);
       }
+      __syncwarp();
     }
-    __syncwarp();
-  } else {
-    // ================================================== compute warps
-    const int g = lane >> 2, cq = lane & 3;
-    uint32_t cc = 0;
-    bool alive = true;
-    for (int item = blockIdx.x; item < total && alive; item += gridDim.x) {
-      const int4 t = __ldg(a.tiles + first + item / n_wtiles);
-      const int wt = item % n_wtiles;
-      const int nw = min(kTN, a.N_out - wt * kTN);
-      const bool rows_ok = (unsigned)t.x < (unsigned)a.E && t.y >= 0 && t.z > 0 &&
-                           t.z <= kSmallRows && (int64_t)t.y + t.z <= a.rows_max;
-      const int64_t off = rows_ok ? __ldg(a.eoff + 2 * t.x + a.which) : -1;
-      if (!(rows_ok && off >= 0 && (off & 15) == 0 && off + mbytes <= a.pack_bytes)) {
-        if (tid == 0) atomicOr(a.status, MOE_STATUS_BAD_OFFSET);
-        continue;
-      }
+  };
+
+  const int g = lane >> 2, cq = lane & 3;
+  uint32_t cc = 0;
+  uint32_t xc = 0;  // amax exchanges of this warp's pair so far
+  bool alive = true;
+  for (int item = blockIdx.x; item < total && alive; item += gridDim.x) {
+    const ItemInfo I = item_info(a, first, n_wtiles, mbytes, item);
+    if (!I.ok) {
+      if (tid == 0) atomicOr(a.status, MOE_STATUS_BAD_OFFSET);
+      continue;
+    }
+    const int4 t = I.t;
+    const int wt = I.wt, nw = I.nw;
+    {
       const int u = t.z;
-      const int nnt = (u + 7) >> 3;  // n8 fragments of routed rows (1 or 2)
-      // tile rows of m16 fragment mt: down 64w + 16mt; gate/up (tile = nwg
-      // gate rows then the matching nwg up rows) gate 32w + 16mt (mt 0,1),
-      // up nwg + 32w + 16(mt-2) (mt 2,3)
+      const int nnt = (u + 7) >> 3;  // n8 fragments of routed rows (1 to 4)
+      // tile rows of m16 fragment mt: down 32w + 16mt; gate/up (tile = nwg
+      // gate rows then the matching nwg up rows) gate 16w (mt 0), up nwg + 16w
+      // (mt 1) -- the warp holds both halves of outputs 16w .. 16w+15
       const int nwg = nw >> 1;
-      int rbase[4];
-      bool mact[4];
+      const int rbase[2] = {kDown ? 32 * warp : 16 * warp, kDown ? 32 * warp + 16 : nwg + 16 * warp};
+      const bool active = kDown ? 32 * warp < nw : 16 * warp < nwg;  // warp-uniform
+      float acc[2][4][4];
 #pragma unroll
-      for (int mt = 0; mt < 4; mt++) {
-        rbase[mt] = kDown ? 64 * warp + 16 * mt
-                          : (mt < 2 ? 32 * warp + 16 * mt : nwg + 32 * warp + 16 * (mt - 2));
-        mact[mt] = kDown ? rbase[mt] < nw : 32 * warp + 16 * (mt & 1) < nwg;
-      }
-      float acc[4][2][4];
+      for (int mt = 0; mt < 2; mt++)
 #pragma unroll
-      for (int mt = 0; mt < 4; mt++)
-#pragma unroll
-        for (int nt = 0; nt < 2; nt++)
+        for (int nt = 0; nt < 4; nt++)
 #pragma unroll
           for (int i = 0; i < 4; i++) acc[mt][nt][i] = 0.0f;
-      alive = nnt == 1 ? consume_item<FMT, 1>(smem, full, empty, s_abort, cc, nchunks, a.bpr, nw,
-                                              rbase, s_lut, lane, acc)
-                       : consume_item<FMT, 2>(smem, full, empty, s_abort, cc, nchunks, a.bpr, nw,
-                                              rbase, s_lut, lane, acc);
+#define MOE_SMALL_CONSUME(N)                                                                  \
+  consume_item<FMT, N>(smem, full, empty, s_abort, cc, nchunks, a.bpr, nw, rbase, s_lut, lane, \
+                       acc, refill)
+      alive = nnt == 1   ? MOE_SMALL_CONSUME(1)
+              : nnt == 2 ? MOE_SMALL_CONSUME(2)
+              : nnt == 3 ? MOE_SMALL_CONSUME(3)
+                         : MOE_SMALL_CONSUME(4);
+#undef MOE_SMALL_CONSUME
       if (!alive) break;
 
       // ---- store.  C fragment: rows g, g+8 of the m16 tile, routed rows
       // 8nt + 2cq, +1 (only rows < u are real)
       if (kDown) {
+        if (!active) continue;
 #pragma unroll
-        for (int mt = 0; mt < 4; mt++) {
-          if (!mact[mt]) continue;
+        for (int mt = 0; mt < 2; mt++) {
 #pragma unroll
-          for (int nt = 0; nt < 2; nt++) {
+          for (int nt = 0; nt < 4; nt++) {
 #pragma unroll
             for (int i = 0; i < 4; i++) {
               const int rr = 8 * nt + 2 * cq + (i & 1);
-              const int o = wt * kTN + rbase[mt] + g + 8 * (i >> 1);
-              if (nt < nnt && rr < u) a.out[(int64_t)(t.y + rr) * a.N_out + o] = acc[mt][nt][i];
+              const int r = rbase[mt] + g + 8 * (i >> 1);
+              if (rr < u && r < nw) a.out[(int64_t)(t.y + rr) * a.N_out + wt * kTN + r] = acc[mt][nt][i];
             }
           }
         }
       } else if (MODE == kModeGU) {
+        if (!active) continue;
         const int n_ff = a.N_out >> 1;
+        // gate and up outputs 128t + 16w + g (+8)
+        const int o = wt * (kTN / 2) + 16 * warp + g;
 #pragma unroll
-        for (int mt = 0; mt < 4; mt++) {
-          if (!mact[mt]) continue;
-          // gate and up outputs 128t + 32w + 16(mt&1) + g (+8)
-          const int o = wt * (kTN / 2) + 32 * warp + 16 * (mt & 1) + (mt < 2 ? 0 : n_ff);
+        for (int nt = 0; nt < 4; nt++)
 #pragma unroll
-          for (int nt = 0; nt < 2; nt++)
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-              const int rr = 8 * nt + 2 * cq + (i & 1);
-              if (nt < nnt && rr < u)
-                a.out[(int64_t)(t.y + rr) * a.N_out + o + g + 8 * (i >> 1)] = acc[mt][nt][i];
-            }
-        }
-      } else {
-        // swiglu_quant fused: the warp holds outputs 128t + 32w .. + 31 (one
-        // q8 block of H) for each routed row: 4 values a thread (fragments
-        // 0,1 x rows g, g+8), the block across the 8 lanes of equal cq
-        const int n_ff = a.N_out >> 1;
-        const int o = wt * (kTN / 2) + 32 * warp;
-        if (32 * warp < nwg) {
-#pragma unroll
-          for (int nt = 0; nt < 2; nt++) {
-            if (nt >= nnt) continue;
-#pragma unroll
-            for (int col = 0; col < 2; col++) {
-              float h[4];  // (fragment 0 row g, fragment 0 row g+8, fragment 1 row g, row g+8)
-              float amax = 0.0f;
-#pragma unroll
-              for (int k = 0; k < 4; k++) {
-                const int mt = k >> 1, i = 2 * (k & 1) + col;
-                const float gv = acc[mt][nt][i], uv = acc[mt + 2][nt][i];
-                h[k] = __fmul_rn(__fdiv_rn(gv, __fadd_rn(1.0f, expf(-gv))), uv);
-                amax = fmaxf(amax, fabsf(h[k]));
-              }
-              amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-              amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
-              amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
-              const float d = __fdiv_rn(amax, 127.0f);
-              const int rr = 8 * nt + 2 * cq + col;
-              if (rr < u) {
-                __half* hrow = a.hq + (int64_t)(t.y + rr) * n_ff + o;
-#pragma unroll
-                for (int mt = 0; mt < 2; mt++) {
-                  // 16-value group mt: position 2g holds value g, 2g+1 value g+8
-                  const float q0 = (d == 0.0f) ? 0.0f : rintf(__fdiv_rn(h[2 * mt], d));
-                  const float q1 = (d == 0.0f) ? 0.0f : rintf(__fdiv_rn(h[2 * mt + 1], d));
-                  *reinterpret_cast<__half2*>(hrow + 16 * mt + 2 * g) = __floats2half2_rn(q0, q1);
-                }
-                if (g == 0) a.dh[(int64_t)(t.y + rr) * scale_stride(n_ff) + (o >> 5)] = d;
-              }
+          for (int i = 0; i < 4; i++) {
+            const int rr = 8 * nt + 2 * cq + (i & 1);
+            if (rr < u) {
+              float* orow = a.out + (int64_t)(t.y + rr) * a.N_out + o + 8 * (i >> 1);
+              orow[0] = acc[0][nt][i];
+              orow[n_ff] = acc[1][nt][i];
             }
           }
-        }
+      } else {
+        // swiglu_quant fused: the warp holds outputs 128t + 16w .. +15 (one
+        // 16-value group; the q8 block of H is this warp's group and its pair
+        // warp's), 2 values a thread per routed row: outputs g and g+8, exactly
+        // the stored pair (positions 2g, 2g+1) of the group.  The pair's amax
+        // goes through shared memory, double-buffered by exchange parity
+        // (a warp cannot run two exchanges ahead of its pair).  Warps are
+        // active in pairs: nwg is a multiple of 64.
+        if (!active) continue;
+        const int n_ff = a.N_out >> 1;
+        const int o = wt * (kTN / 2) + 16 * warp;
+        const uint32_t xb = xc & 1;
+        float* am_own = s_amax + (xb * kWarps + warp) * kRows;
+        const float* am_pair = s_amax + (xb * kWarps + (warp ^ 1)) * kRows;
+        float hv[4][2][2];  // [nt][col][output g / g+8]
+        float am[4][2];
+#pragma unroll
+        for (int nt = 0; nt < 4; nt++)
+#pragma unroll
+          for (int col = 0; col < 2; col++) {
+            float amax = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 2; e++) {
+              const int i = 2 * e + col;
+              const float gv = acc[0][nt][i], uv = acc[1][nt][i];
+              hv[nt][col][e] = __fmul_rn(__fdiv_rn(gv, __fadd_rn(1.0f, expf(-gv))), uv);
+              amax = fmaxf(amax, fabsf(hv[nt][col][e]));
+            }
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
+            am[nt][col] = amax;
+            if (g == 0) am_own[8 * nt + 2 * cq + col] = amax;
+          }
+        uint64_t* pb = &pairbar[xb * (kWarps / 2) + (warp >> 1)];
+        mbar_arrive(pb);
+        if (!(alive = mbar_wait(pb, (xc >> 1) & 1, s_abort, kTimeoutNs, false))) break;
+        xc++;
+#pragma unroll
+        for (int nt = 0; nt < 4; nt++)
+#pragma unroll
+          for (int col = 0; col < 2; col++) {
+            const int rr = 8 * nt + 2 * cq + col;
+            const float d = __fdiv_rn(fmaxf(am[nt][col], am_pair[rr]), 127.0f);
+            if (rr < u) {
+              const float q0 = (d == 0.0f) ? 0.0f : rintf(__fdiv_rn(hv[nt][col][0], d));
+              const float q1 = (d == 0.0f) ? 0.0f : rintf(__fdiv_rn(hv[nt][col][1], d));
+              __half* hrow = a.hq + (int64_t)(t.y + rr) * n_ff + o;
+              *reinterpret_cast<__half2*>(hrow + 2 * g) = __floats2half2_rn(q0, q1);
+              if (g == 0 && (warp & 1) == 0)
+                a.dh[(int64_t)(t.y + rr) * scale_stride(n_ff) + (o >> 5)] = d;
+            }
+          }
       }
     }
   }
+  // copies still in flight after an abort land before the CTA exits
+  if (tid == 0)
+    for (uint32_t i = cc; i < prod.issued; i++)
+      if (!mbar_wait(&full[i % kSlots], (i / kSlots) & 1, s_abort, kTimeoutNs, false)) break;
   if (*s_abort && tid == 0) atomicOr(a.status, MOE_STATUS_PIPE_TIMEOUT);
 }
 
@@ -462,18 +523,32 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_small() {
   return fn;
 }
 
+// Resident CTAs a multiprocessor (two by design), found once per device.
 template <int FMT, int MODE>
-cudaError_t launch_small(const SmArgs& a, const CUtensorMap& tm, const CUtensorMap& td, int grid,
-                         cudaStream_t st) {
-  static bool done[64] = {false};
+cudaError_t launch_small(const SmArgs& a, const CUtensorMap& tm, const CUtensorMap& td,
+                         int64_t items, cudaStream_t st) {
+  static int per_sm[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !done[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!per_sm[dev]) {
+    // two CTAs a multiprocessor: the full shared-memory carveout
+    cudaError_t e = cudaFuncSetAttribute(
         gemm_small_kernel<FMT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_small_kernel<FMT, MODE>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
+    int n = 0;
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemm_small_kernel<FMT, MODE>, kThreads,
+                                                         kSmemBytes);
     if (e != cudaSuccess) return e;
-    done[dev] = true;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    per_sm[dev] = n;
   }
+  const int grid =
+      (int)std::max<int64_t>(1, std::min<int64_t>(items, (int64_t)per_sm[dev] * device_sm_count()));
   gemm_small_kernel<FMT, MODE><<<grid, kThreads, kSmemBytes, st>>>(a, tm, td);
   return cudaSuccess;
 }
@@ -507,7 +582,7 @@ cudaError_t launch_gemm_small(const GemmArgs& g, cudaStream_t st) {
   CUtensorMap tm, td;
   const cuuint64_t dims[2] = {(cuuint64_t)g.K, (cuuint64_t)g.rows_max};
   const cuuint64_t strides[1] = {(cuuint64_t)g.K * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kActBox, (cuuint32_t)kSmallRows};
+  const cuuint32_t box[2] = {(cuuint32_t)kActBox, (cuuint32_t)kBoxRows};
   const cuuint32_t estr[2] = {1, 1};
   if (encode(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(g.act), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -517,26 +592,26 @@ cudaError_t launch_gemm_small(const GemmArgs& g, cudaStream_t st) {
   const int ss = scale_stride(g.K);
   const cuuint64_t ddims[2] = {(cuuint64_t)ss, (cuuint64_t)g.rows_max};
   const cuuint64_t dstrides[1] = {(cuuint64_t)ss * 4};
-  const cuuint32_t dbox[2] = {(cuuint32_t)(vals / 32), (cuuint32_t)kSmallRows};
+  const cuuint32_t dbox[2] = {(cuuint32_t)(vals / 32), (cuuint32_t)kBoxRows};
   if (encode(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(g.act_d), ddims, dstrides,
              dbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
 
-  // one item per (small expert, 256-row weight tile); two CTAs a multiprocessor
+  // one item per (small-row tile, 256-row weight tile)
   const int64_t n_wtiles = (g.N_out + kTN - 1) / kTN;
-  const int64_t items_max = (int64_t)std::min<int64_t>(g.E, g.rows_max) * n_wtiles;
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(items_max, 2 * device_sm_count()));
+  const int64_t items_max =
+      (int64_t)std::min<int64_t>((int64_t)g.E * (kSmallSplit / kSmallTileRows), g.rows_max) * n_wtiles;
   const int mode = g.which == 1 ? kModeDown : (g.hq ? kModeSwiglu : kModeGU);
   cudaError_t e;
   if (g.fmt == MOE_FMT_W2) {
-    e = mode == kModeDown     ? launch_small<MOE_FMT_W2, kModeDown>(a, tm, td, grid, st)
-        : mode == kModeSwiglu ? launch_small<MOE_FMT_W2, kModeSwiglu>(a, tm, td, grid, st)
-                              : launch_small<MOE_FMT_W2, kModeGU>(a, tm, td, grid, st);
+    e = mode == kModeDown     ? launch_small<MOE_FMT_W2, kModeDown>(a, tm, td, items_max, st)
+        : mode == kModeSwiglu ? launch_small<MOE_FMT_W2, kModeSwiglu>(a, tm, td, items_max, st)
+                              : launch_small<MOE_FMT_W2, kModeGU>(a, tm, td, items_max, st);
   } else {
-    e = mode == kModeDown     ? launch_small<MOE_FMT_W4NL, kModeDown>(a, tm, td, grid, st)
-        : mode == kModeSwiglu ? launch_small<MOE_FMT_W4NL, kModeSwiglu>(a, tm, td, grid, st)
-                              : launch_small<MOE_FMT_W4NL, kModeGU>(a, tm, td, grid, st);
+    e = mode == kModeDown     ? launch_small<MOE_FMT_W4NL, kModeDown>(a, tm, td, items_max, st)
+        : mode == kModeSwiglu ? launch_small<MOE_FMT_W4NL, kModeSwiglu>(a, tm, td, items_max, st)
+                              : launch_small<MOE_FMT_W4NL, kModeGU>(a, tm, td, items_max, st);
   }
   if (e != cudaSuccess) return e;
   count_launch();

@@ -307,8 +307,9 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
   constexpr int kSpc = kChunkBlocks / kBps;            // stages per raw chunk
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  // 1024-byte aligned base, offset from the shared array itself (an integer
+  // round trip would hide the shared address space from the compiler)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = smem + kOffA;
   uint8_t* sB = smem + kOffB;
   uint8_t* sRaw = smem + kOffRaw;

@@ -10,8 +10,9 @@
 //                       base row of every (chunk, expert), the expert counts,
 //                       their exclusive prefix sum (group bounds), the
 //                       largest-first expert order, and the product kernels'
-//                       work list: every expert's rows cut into tiles of at
-//                       most 128 rows, largest expert first;
+//                       work list: every expert's rows cut into 128-row
+//                       tiles, largest expert first, a short remainder cut
+//                       into 32-row tiles for the small-row tier;
 //   3. route_scatter -- each warp walks its chunk again, 32 entries at a
 //                       time; __match_any_sync groups lanes of equal expert,
 //                       a lane's rank among them keeps flat order, so rows of
@@ -81,11 +82,11 @@ route_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E,
                   int32_t* __restrict__ order, int4* __restrict__ tiles,
                   int32_t* __restrict__ ntiles) {
   __shared__ int32_t s_cnt[1024];    // rows of expert e
-  __shared__ int32_t s_tiles[1024];  // tiles of the expert at rank r
+  __shared__ int32_t s_tiles[1024];  // tcgen05 tiles of the expert at rank r
+  __shared__ int32_t s_small[1024];  // small-row tiles of the expert at rank r
   __shared__ int32_t s_warp[32];
-  __shared__ int32_t s_big;  // tiles of experts with more than kSmallRows rows
+  __shared__ int32_t s_tot[2];       // tcgen05 tiles, small-row tiles
   const int tid = threadIdx.x;
-  if (tid == 0) s_big = 0;
   int run = 0;
   if (tid < E) {
     for (int c = 0; c < nchunks; c++) {
@@ -98,8 +99,15 @@ route_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E,
   }
   s_cnt[tid] = run;
   s_tiles[tid] = 0;
+  s_small[tid] = 0;
   const int excl = block_excl_scan(run, s_warp);  // also orders s_cnt / s_tiles writes
   int rank = 0;
+  // this expert's tiles: full 128-row tiles, then the remainder -- one more
+  // tcgen05 tile, or 32-row small-row tiles when it is at most kSmallSplit rows
+  const int nfull = run / kTileRows, rem = run - nfull * kTileRows;
+  const bool rem_small = rem > 0 && rem <= kSmallSplit;
+  const int nbig = nfull + (rem > 0 && !rem_small ? 1 : 0);
+  const int nsm = rem_small ? (rem + kSmallTileRows - 1) / kSmallTileRows : 0;
   if (tid < E) {
     offsets[tid] = excl;
     if (tid == E - 1) offsets[E] = excl + run;
@@ -110,24 +118,33 @@ route_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E,
       rank += (c2 > run) || (c2 == run && e2 < tid);
     }
     order[rank] = tid;
-    s_tiles[rank] = (run + kTileRows - 1) / kTileRows;
-    if (run > kSmallRows) atomicAdd(&s_big, (run + kTileRows - 1) / kTileRows);
+    s_tiles[rank] = nbig;
+    s_small[rank] = nsm;
   }
   __syncthreads();
-  // first tile of each rank (thread tid stands for rank tid here)
-  const int nt = s_tiles[tid];
+  // first tile of each rank in each list (thread tid stands for rank tid here)
+  const int nt = s_tiles[tid], ns = s_small[tid];
   const int tbase = block_excl_scan(nt, s_warp);
+  const int sbase = block_excl_scan(ns, s_warp);
   if (tid == 1023) {
-    ntiles[0] = tbase + nt;
-    ntiles[1] = s_big;  // the big experts' tiles come first (largest first)
+    s_tot[0] = tbase + nt;
+    s_tot[1] = sbase + ns;
+    ntiles[0] = tbase + nt + sbase + ns;
+    ntiles[1] = tbase + nt;  // the tcgen05 tiles come first
   }
   __syncthreads();
   s_tiles[tid] = tbase;
+  s_small[tid] = s_tot[0] + sbase;
   __syncthreads();
   if (tid < E) {
     const int first = s_tiles[rank];
-    for (int i = 0; i * kTileRows < run; i++)
+    for (int i = 0; i < nbig; i++)
       tiles[first + i] = make_int4(tid, excl + i * kTileRows, min(kTileRows, run - i * kTileRows), 0);
+    const int sfirst = s_small[rank];
+    const int r0 = excl + nfull * kTileRows;
+    for (int j = 0; j < nsm; j++)
+      tiles[sfirst + j] = make_int4(tid, r0 + j * kSmallTileRows,
+                                    min(kSmallTileRows, rem - j * kSmallTileRows), 0);
   }
 }
 
