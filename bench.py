@@ -42,11 +42,12 @@ FP32_LANES_PER_SM = 128
 # GB300 (tcgen05 kind::i8 does not exist there); MEASURED_PEAKS.json has no
 # int8 figure
 INT8_MMA_PEAK_TOPS = 150.0
-# DRAM bytes of one gate/up launch at configuration 2 (ncu, one pass:
-# profiles/dram_gemm_tc_T16384.md), valid while the product kernel's sources
-# hash as they did at capture
-TRAFFIC_GATE_UP = {2: 1.646e9}
-TRAFFIC_SOURCES_SHA = "2160ac2cd09e3e29"
+# DRAM bytes of one gate/up stage (the tcgen05 launch plus the small-row
+# launch) at configuration 2 (ncu, one pass: profiles/dram_gate_up_T16384.md),
+# valid while the product kernels' sources hash as they did at capture
+TRAFFIC_GATE_UP = {2: 1.5878e9}
+TRAFFIC_SOURCES_SHA = "bc34e9a168897525"
+TRAFFIC_SOURCES = ("gemm_tc.cu", "gemm_small.cu", "route.cu", "sm100_ptx.cuh", "common.cuh")
 ALGO_BYTES_GATE_UP = {2: 1.586e9}
 
 
@@ -54,7 +55,7 @@ def measured_traffic(config: int):
     import hashlib
     csrc = os.path.join(ROOT, "quantized_moe_expert_quantize_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("gemm_tc.cu", "sm100_ptx.cuh", "common.cuh"):
+    for f in TRAFFIC_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     if h.hexdigest()[:16] != TRAFFIC_SOURCES_SHA:
@@ -338,15 +339,17 @@ def run_ours(args):
                          "intermediates > 2.5 GB) through a 129 MB L2"},
         "effective_int8_tops": eff_tops,
         "stage_ms": stage_ms,
-        "roofline": {"bound": "tensor", "kernel": "gate_up_swiglu", "achieved": achieved,
+        "roofline": {"bound": "tensor",
+                     "kernel": "gate_up_swiglu (tcgen05 launch + small-row launch)",
+                     "achieved": achieved,
                      "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["bf16_sustained"], "traffic": traffic,
                      "peak_source": peaks["source"] + " bf16 dense, sustained (the kernel is "
                                     "timed inside the layer's steps); fp16 operands run at "
                                     "the bf16 rate",
-                     "algorithmic": f"2*R*2*n_ff*d = {gu_flops:.4g} flop per launch; "
+                     "algorithmic": f"2*R*2*n_ff*d = {gu_flops:.4g} flop per stage; "
                                     f"{ALGO_BYTES_GATE_UP.get(args.config, float('nan')):.4g} "
-                                    "algorithmic bytes per launch",
+                                    "algorithmic bytes per stage",
                      "launch_ms": gu_ms},
         "roofline_alu": {"bound": "alu", "kernel": "gate_up_swiglu", "achieved": alu_achieved,
                          "peak": alu_peak, "unit": "T fp32 lane-ops/s",
