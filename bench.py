@@ -68,6 +68,30 @@ def ops_per_row(s: synth.LayerShape) -> int:
     return 2 * (2 * s.n_ff * s.d + s.d * s.n_ff)
 
 
+def layer_bytes(L) -> dict:
+    """Algorithmic HBM bytes of one layer step: the weights of the experts the
+    routing touches, x, the routing, out, and the staged intermediates (q8 of
+    x and H with their scales, Dm), each written once and read once."""
+    s = L.shape
+    R = s.T * s.k
+    touched = np.unique(L.topk_ids.reshape(-1))
+    touched = touched[(touched >= 0) & (touched < s.E)]
+    g = synth.row_bytes(s.gu_fmt, s.d) * 2 * s.n_ff
+    dn = synth.row_bytes(s.down_fmt, s.n_ff) * s.d
+    sd, sf = ((s.d // 32 + 3) & ~3), ((s.n_ff // 32 + 3) & ~3)
+    parts = {
+        "weights": len(touched) * (g + dn),
+        "x": s.T * s.d * 4,
+        "routing": s.T * s.k * 8,
+        "out": s.T * s.d * 4,
+        "xq+dx": 2 * R * (s.d * 2 + sd * 4),
+        "hq+dh": 2 * R * (s.n_ff * 2 + sf * 4),
+        "dm": 2 * R * s.d * 4,
+    }
+    parts["total"] = sum(parts.values())
+    return parts
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -326,6 +350,7 @@ def run_ours(args):
     alu_achieved = 2.0 * pairs / (gu_ms * 1e-3) / 1e12
     eff_tops = value * s.k * ops_per_row(s) / 1e12
     traffic = measured_traffic(args.config)
+    hbm = layer_bytes(L)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -355,6 +380,13 @@ def run_ours(args):
                          "peak": alu_peak, "unit": "T fp32 lane-ops/s",
                          "frac": alu_achieved / alu_peak,
                          "algorithmic": "2 ops (mul, fma) per (output, 32-value block)"},
+        "roofline_hbm": {"bound": "hbm", "kernel": "layer (all launches of a step)",
+                         "achieved": hbm["total"] / (ms_per_step * 1e-3) / 1e9,
+                         "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": hbm["total"] / (ms_per_step * 1e-3) / 1e9 / peaks["hbm"],
+                         "algorithmic_bytes": hbm,
+                         "note": "binds at small T (the weight stream); at large T the "
+                                 "products' tensor and epilogue rooflines bind"},
         "roofline_int8": {"bound": "tensor (int8)", "kernel": "layer",
                           "achieved": eff_tops, "peak": INT8_MMA_PEAK_TOPS, "unit": "TOPS",
                           "frac": eff_tops / INT8_MMA_PEAK_TOPS,

@@ -2,6 +2,7 @@
 // order of the stages.  See include/moe_prefill.h for the contract.
 #include <atomic>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -122,6 +123,44 @@ int open_ctx(const MoeLayerDesc* desc, void* workspace, size_t bytes, Ctx& c) {
 
 inline int launch_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH; }
 
+// A second stream per device for the small-row launch, so that it runs
+// beside the tcgen05 launch (the two read the same inputs and write disjoint
+// rows) and fills the multiprocessors the tcgen05 tiles leave idle.  It
+// forks from the caller's stream and joins back before the call returns, so
+// to the caller the stage is ordered on its own stream as before (also under
+// stream capture, where the fork and join become graph edges).  One stream
+// and two events per device, created on the first call that is not being
+// captured and kept until the process exits; calls enqueue under a lock, as
+// the events are shared.  Without them the two launches share the caller's
+// stream.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool tried = false;
+};
+std::mutex g_side_mu;
+SideStream g_side[64];
+
+SideStream* side_stream(cudaStream_t st) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  SideStream& sd = g_side[dev];
+  if (!sd.s && !sd.tried) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+      return nullptr;
+    sd.tried = true;
+    if (cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      sd.s = nullptr;
+      return nullptr;
+    }
+  }
+  return sd.s ? &sd : nullptr;
+}
+
 // The status word starts every layer (and every moe_route) at zero.
 int run_route(Ctx& c, const int32_t* ids, cudaStream_t st) {
   if (cudaMemsetAsync(c.v.status, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_LAUNCH;
@@ -166,10 +205,21 @@ int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaSt
     a.out = c.v.dm;
   }
   // 128-row tiles on the tcgen05 kernel, short remainders on the small-row
-  // tier (both read the tile list's split point on the device)
+  // tier (both read the tile list's split point on the device), the latter
+  // on the side stream when there is one
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  SideStream* sd = side_stream(st);
+  if (sd && (cudaEventRecord(sd->fork, st) != cudaSuccess ||
+             cudaStreamWaitEvent(sd->s, sd->fork, 0) != cudaSuccess))
+    return MOE_ERR_LAUNCH;
   const cudaError_t e = launch_gemm_tc(a, st);
-  if (e != cudaSuccess) return launch_rc(e);
-  return launch_rc(launch_gemm_small(a, st));
+  const cudaError_t e2 = e == cudaSuccess ? launch_gemm_small(a, sd ? sd->s : st) : e;
+  // always join, so that a failed launch leaves no open fork (nor an unjoined
+  // stream in a capture)
+  if (sd && (cudaEventRecord(sd->join, sd->s) != cudaSuccess ||
+             cudaStreamWaitEvent(st, sd->join, 0) != cudaSuccess))
+    return MOE_ERR_LAUNCH;
+  return launch_rc(e2);
 }
 
 int run_swiglu(Ctx& c, cudaStream_t st) {
