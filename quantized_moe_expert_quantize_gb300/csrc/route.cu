@@ -3,7 +3,10 @@
 // ("Strata #3752", commits "moe_ws wiring" and "swiglu_quant landed":
 // quantize_scatter, the group bounds uploaded with the layer).
 //
-// Three small kernels, all integer and bit-exact:
+// All integer and bit-exact.  Up to 2^14 entries (T*k) one kernel does it all
+// in one CTA (route_fused: 32 warps, each counting and then placing a
+// contiguous 1/32 of the entries with its counts in shared memory); a launch
+// saved matters more there than parallelism.  Beyond that, three kernels:
 //   1. route_hist    -- one warp per chunk of 1024 flat entries counts the
 //                       chunk's rows per expert (shared-memory histogram);
 //   2. route_scan    -- one CTA turns the [chunk][expert] counts into the
@@ -36,11 +39,19 @@ route_hist_kernel(const int32_t* __restrict__ ids, int64_t n, int E, int nchunks
   __syncwarp();
   const int64_t beg = (int64_t)chunk * kRouteChunk;
   const int64_t end = min(n, beg + kRouteChunk);
+  // all of this lane's ids first (independent loads), then the counts
+  int v[kRouteChunk / 32];
+#pragma unroll
+  for (int j = 0; j < kRouteChunk / 32; j++) {
+    const int64_t i = beg + lane + 32 * j;
+    v[j] = i < end ? __ldg(ids + i) : 0;
+  }
   bool bad = false;
-  for (int64_t i = beg + lane; i < end; i += 32) {
-    const int e = ids[i];
-    if ((unsigned)e < (unsigned)E)
-      atomicAdd(&h[e], 1);
+#pragma unroll
+  for (int j = 0; j < kRouteChunk / 32; j++) {
+    if (beg + lane + 32 * j >= end) break;
+    if ((unsigned)v[j] < (unsigned)E)
+      atomicAdd(&h[v[j]], 1);
     else
       bad = true;
   }
@@ -75,32 +86,27 @@ __device__ __forceinline__ int block_excl_scan(int v, int32_t* s_warp) {
   return s_warp[warp] + incl - v;
 }
 
-// One CTA of 1024 threads; thread e owns expert e (E <= 1024).
-__global__ void __launch_bounds__(1024)
-route_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E,
-                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                  int32_t* __restrict__ order, int4* __restrict__ tiles,
-                  int32_t* __restrict__ ntiles) {
-  __shared__ int32_t s_cnt[1024];    // rows of expert e
-  __shared__ int32_t s_tiles[1024];  // tcgen05 tiles of the expert at rank r
-  __shared__ int32_t s_small[1024];  // small-row tiles of the expert at rank r
-  __shared__ int32_t s_warp[32];
-  __shared__ int32_t s_tot[2];       // tcgen05 tiles, small-row tiles
+// Per-expert lists, run by one CTA of 1024 threads, thread e standing for
+// expert e (E <= 1024) with run = its row count: counts, the group bounds
+// (returned: the expert's first routed row), the largest-first order and
+// the work list of tiles with its split count.
+struct ScanShared {
+  __align__(16) int32_t cnt[1024];  // rows of expert e (0 past E)
+  int32_t tiles[1024];              // tcgen05 tiles of the expert at rank r, then their first
+  int32_t small[1024];              // small-row tiles of the expert at rank r, then their first
+  int32_t warp[32];
+  int32_t tot[2];                   // tcgen05 tiles, small-row tiles
+};
+__device__ __forceinline__ int expert_lists(int run, int E, int32_t* __restrict__ counts,
+                                            int32_t* __restrict__ offsets,
+                                            int32_t* __restrict__ order, int4* __restrict__ tiles,
+                                            int32_t* __restrict__ ntiles, ScanShared& sh) {
   const int tid = threadIdx.x;
-  int run = 0;
-  if (tid < E) {
-    for (int c = 0; c < nchunks; c++) {
-      const int64_t idx = (int64_t)c * E + tid;
-      const int v = hist[idx];
-      hist[idx] = run;  // rows of expert tid in chunks before c
-      run += v;
-    }
-    counts[tid] = run;
-  }
-  s_cnt[tid] = run;
-  s_tiles[tid] = 0;
-  s_small[tid] = 0;
-  const int excl = block_excl_scan(run, s_warp);  // also orders s_cnt / s_tiles writes
+  if (tid < E) counts[tid] = run;
+  sh.cnt[tid] = run;
+  sh.tiles[tid] = 0;
+  sh.small[tid] = 0;
+  const int excl = block_excl_scan(run, sh.warp);  // also orders the writes above
   int rank = 0;
   // this expert's tiles: full 128-row tiles, then the remainder -- one more
   // tcgen05 tile, or 32-row small-row tiles when it is at most kSmallSplit rows
@@ -111,41 +117,165 @@ route_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E,
   if (tid < E) {
     offsets[tid] = excl;
     if (tid == E - 1) offsets[E] = excl + run;
-    for (int c = 0; c < nchunks; c++) hist[(int64_t)c * E + tid] += excl;
-    // rank by (count descending, id ascending)
-    for (int e2 = 0; e2 < E; e2++) {
-      const int c2 = s_cnt[e2];
-      rank += (c2 > run) || (c2 == run && e2 < tid);
+    // rank by (count descending, id ascending); cnt past E is 0 with ids
+    // above every expert's, so whole int4 reads count nothing extra
+    for (int e2 = 0; e2 < E; e2 += 4) {
+      const int4 c4 = *reinterpret_cast<const int4*>(sh.cnt + e2);
+      rank += (c4.x > run) || (c4.x == run && e2 < tid);
+      rank += (c4.y > run) || (c4.y == run && e2 + 1 < tid);
+      rank += (c4.z > run) || (c4.z == run && e2 + 2 < tid);
+      rank += (c4.w > run) || (c4.w == run && e2 + 3 < tid);
     }
     order[rank] = tid;
-    s_tiles[rank] = nbig;
-    s_small[rank] = nsm;
+    sh.tiles[rank] = nbig;
+    sh.small[rank] = nsm;
   }
   __syncthreads();
   // first tile of each rank in each list (thread tid stands for rank tid here)
-  const int nt = s_tiles[tid], ns = s_small[tid];
-  const int tbase = block_excl_scan(nt, s_warp);
-  const int sbase = block_excl_scan(ns, s_warp);
+  const int nt = sh.tiles[tid], ns = sh.small[tid];
+  const int tbase = block_excl_scan(nt, sh.warp);
+  const int sbase = block_excl_scan(ns, sh.warp);
   if (tid == 1023) {
-    s_tot[0] = tbase + nt;
-    s_tot[1] = sbase + ns;
+    sh.tot[0] = tbase + nt;
+    sh.tot[1] = sbase + ns;
     ntiles[0] = tbase + nt + sbase + ns;
     ntiles[1] = tbase + nt;  // the tcgen05 tiles come first
   }
   __syncthreads();
-  s_tiles[tid] = tbase;
-  s_small[tid] = s_tot[0] + sbase;
+  sh.tiles[tid] = tbase;
+  sh.small[tid] = sh.tot[0] + sbase;
   __syncthreads();
   if (tid < E) {
-    const int first = s_tiles[rank];
+    const int first = sh.tiles[rank];
     for (int i = 0; i < nbig; i++)
       tiles[first + i] = make_int4(tid, excl + i * kTileRows, min(kTileRows, run - i * kTileRows), 0);
-    const int sfirst = s_small[rank];
+    const int sfirst = sh.small[rank];
     const int r0 = excl + nfull * kTileRows;
     for (int j = 0; j < nsm; j++)
       tiles[sfirst + j] = make_int4(tid, r0 + j * kSmallTileRows,
                                     min(kSmallTileRows, rem - j * kSmallTileRows), 0);
   }
+  return excl;
+}
+
+// One CTA of 1024 threads; thread e owns expert e (E <= 1024).
+__global__ void __launch_bounds__(1024)
+route_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E,
+                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                  int32_t* __restrict__ order, int4* __restrict__ tiles,
+                  int32_t* __restrict__ ntiles) {
+  __shared__ ScanShared sh;
+  const int tid = threadIdx.x;
+  int run = 0;
+  if (tid < E) {
+#pragma unroll 8
+    for (int c = 0; c < nchunks; c++) {
+      const int64_t idx = (int64_t)c * E + tid;
+      const int v = hist[idx];
+      hist[idx] = run;  // rows of expert tid in chunks before c
+      run += v;
+    }
+  }
+  const int excl = expert_lists(run, E, counts, offsets, order, tiles, ntiles, sh);
+  if (tid < E) {
+#pragma unroll 8
+    for (int c = 0; c < nchunks; c++) hist[(int64_t)c * E + tid] += excl;
+  }
+}
+
+// Stable placement of entries [beg, end) of ids, 32 at a time in index
+// order: lanes of equal expert are grouped with __match_any_sync and a
+// lane's rank among them keeps flat order; h[e] is the next routed row of
+// expert e for this range.
+__device__ __forceinline__ void scatter_range(const int32_t* __restrict__ ids, int64_t beg,
+                                              int64_t end, int E, int32_t* h,
+                                              int32_t* __restrict__ row_src,
+                                              int32_t* __restrict__ dst_of) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int64_t b0 = beg; b0 < end; b0 += 32 * 8) {
+    int v[8];  // this lane's next 8 ids first (independent loads)
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      const int64_t i = b0 + 32 * j + lane;
+      v[j] = i < end ? __ldg(ids + i) : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      const int64_t base = b0 + 32 * j;
+      if (base >= end) break;
+      const int64_t i = base + lane;
+      const bool act = i < end;
+      const int e = v[j];
+      const bool valid = act && (unsigned)e < (unsigned)E;
+      const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+      const int rank = __popc(peers & lt);
+      const int pos = valid ? h[e] + rank : -1;
+      __syncwarp();
+      if (valid && rank == 0) h[e] += __popc(peers);
+      __syncwarp();
+      if (valid) row_src[pos] = (int32_t)i;
+      if (act) dst_of[i] = pos;
+    }
+  }
+}
+
+// The whole routing step in one CTA of 1024 threads (n <= kFusedMaxEntries):
+// warp w owns the contiguous range [w*S, (w+1)*S) of flat entries (S =
+// ceil(n/32) rounded up to 32) and a shared-memory count per expert.  Counts,
+// then the per-expert lists (with every warp's base for every expert), then
+// the stable scatter -- one launch, the histograms never leave the SM.
+constexpr int kFusedWarps = 32;
+constexpr int64_t kFusedMaxEntries = 1 << 14;
+__global__ void __launch_bounds__(1024)
+route_fused_kernel(const int32_t* __restrict__ ids, int64_t n, int E,
+                   int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                   int32_t* __restrict__ order, int4* __restrict__ tiles,
+                   int32_t* __restrict__ ntiles, int32_t* __restrict__ row_src,
+                   int32_t* __restrict__ dst_of, int32_t* __restrict__ status) {
+  extern __shared__ int32_t hw[];  // [kFusedWarps][E]
+  __shared__ ScanShared sh;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t S = ((n + kFusedWarps - 1) / kFusedWarps + 31) & ~(int64_t)31;
+  const int64_t beg = min(n, (int64_t)warp * S), end = min(n, beg + S);
+  int32_t* h = hw + warp * E;
+  for (int e = lane; e < E; e += 32) h[e] = 0;
+  __syncwarp();
+  bool bad = false;
+  for (int64_t b0 = beg; b0 < end; b0 += 32 * 8) {
+    int v[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      const int64_t i = b0 + 32 * j + lane;
+      v[j] = i < end ? __ldg(ids + i) : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      if (b0 + 32 * j + lane >= end) break;
+      if ((unsigned)v[j] < (unsigned)E)
+        atomicAdd(&h[v[j]], 1);
+      else
+        bad = true;
+    }
+  }
+  if (bad) atomicOr(status, MOE_STATUS_BAD_EXPERT_ID);
+  __syncthreads();
+  int run = 0;
+  if (tid < E) {
+#pragma unroll 8
+    for (int w = 0; w < kFusedWarps; w++) {
+      const int v = hw[w * E + tid];
+      hw[w * E + tid] = run;  // rows of expert tid in ranges before warp w's
+      run += v;
+    }
+  }
+  const int excl = expert_lists(run, E, counts, offsets, order, tiles, ntiles, sh);
+  if (tid < E) {
+#pragma unroll 8
+    for (int w = 0; w < kFusedWarps; w++) hw[w * E + tid] += excl;
+  }
+  __syncthreads();
+  scatter_range(ids, beg, end, E, h, row_src, dst_of);
 }
 
 __global__ void __launch_bounds__(kRouteWarps * 32)
@@ -159,23 +289,8 @@ route_scatter_kernel(const int32_t* __restrict__ ids, int64_t n, int E, int nchu
   if (chunk >= nchunks) return;
   for (int e = lane; e < E; e += 32) h[e] = hist[(int64_t)chunk * E + e];
   __syncwarp();
-  const unsigned lt = (1u << lane) - 1u;
   const int64_t beg = (int64_t)chunk * kRouteChunk;
-  const int64_t end = min(n, beg + kRouteChunk);
-  for (int64_t base = beg; base < end; base += 32) {
-    const int64_t i = base + lane;
-    const bool act = i < end;
-    const int e = act ? ids[i] : -1;
-    const bool valid = act && (unsigned)e < (unsigned)E;
-    const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
-    const int rank = __popc(peers & lt);
-    const int pos = valid ? h[e] + rank : -1;
-    __syncwarp();
-    if (valid && rank == 0) h[e] += __popc(peers);
-    __syncwarp();
-    if (valid) row_src[pos] = (int32_t)i;
-    if (act) dst_of[i] = pos;
-  }
+  scatter_range(ids, beg, min(n, beg + kRouteChunk), E, h, row_src, dst_of);
 }
 
 }  // namespace
@@ -184,6 +299,24 @@ cudaError_t launch_route(const int32_t* ids, int64_t n, int E, int32_t* hist,
                          int32_t* counts, int32_t* offsets, int32_t* order,
                          int32_t* row_src, int32_t* dst_of, int4* tiles, int32_t* ntiles,
                          int32_t* status, cudaStream_t st) {
+  if (n <= kFusedMaxEntries) {
+    // one launch; its per-warp counts take 32*E int32 of shared memory
+    const size_t fsmem = sizeof(int32_t) * kFusedWarps * E;
+    static bool ready[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!ready[dev]) {
+      const cudaError_t e = cudaFuncSetAttribute(
+          route_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+          (int)(sizeof(int32_t) * kFusedWarps * 1024));
+      if (e != cudaSuccess) return e;
+      ready[dev] = true;
+    }
+    route_fused_kernel<<<1, 1024, fsmem, st>>>(ids, n, E, counts, offsets, order, tiles, ntiles,
+                                               row_src, dst_of, status);
+    count_launch();
+    return cudaGetLastError();
+  }
   const int nchunks = route_chunks(n);
   const int grid = (nchunks + kRouteWarps - 1) / kRouteWarps;
   const size_t smem = sizeof(int32_t) * kRouteWarps * E;

@@ -181,6 +181,32 @@ def _layer_with_ids(shape, ids, seed=3, x_override=None):
     return L
 
 
+@pytest.mark.parametrize("T", [1638, 1639, 40000])
+def test_route_both_paths_bit_exact(M, T):
+    """Routing runs in one CTA up to 2^14 flat entries and in three kernels
+    beyond; both give the oracle's counts, bounds, stable permutation and
+    largest-first order bit for bit (T*k = 16,380 / 16,390 / 400,000)."""
+    E, k = 512, 10
+    rng = np.random.default_rng(T)
+    ids_np, _ = synth.draw_topk_routing(rng, T, E, k, True)
+    ids_np[7, 3] = E + 5  # one bad id: dropped and flagged
+    desc = M.make_desc(T, 256, 64, E, k)
+    ws = M.alloc_workspace(desc)
+    M.moe_route(desc, torch.from_numpy(ids_np).cuda(), ws)
+    torch.cuda.synchronize()
+    v = M.workspace_view(desc, ws)
+    counts, offsets, row_src, dst_of, bad = oracle.route(ids_np, E)
+    R = int(offsets[-1])
+    assert bad == 1
+    assert np.array_equal(v["counts"].cpu().numpy(), counts)
+    assert np.array_equal(v["offsets"].cpu().numpy(), offsets)
+    assert np.array_equal(v["row_src"][:R].cpu().numpy(), row_src)
+    assert np.array_equal(v["dst_of"][: T * k].cpu().numpy(), dst_of)
+    want = np.lexsort((np.arange(E), -counts))
+    assert np.array_equal(v["order"].cpu().numpy(), want)
+    assert M.moe_read_status(desc, ws) & M.MOE_STATUS_BAD_EXPERT_ID
+
+
 def test_empty_layer(M):
     shape = synth.LayerShape(0, 256, 64, 8, 2)
     L = synth.make_layer(shape, seed=1)
