@@ -36,7 +36,7 @@ def lib():
         L.orc_expert_rows.restype = None
         L.orc_block_sums.argtypes = [i32, i32, vp, vp, vp]
         L.orc_block_sums.restype = None
-        L.orc_swiglu_quant.argtypes = [i64, i32, vp, vp, vp]
+        L.orc_swiglu_quant.argtypes = [i64, i32, i32, vp, vp, vp]
         L.orc_swiglu_quant.restype = None
         L.orc_combine.argtypes = [i64, i32, i32, vp, vp, vp, vp]
         L.orc_combine.restype = None
@@ -44,7 +44,7 @@ def lib():
         L.orc_row_bytes.restype = i64
         L.orc_w_value.argtypes = [i32, vp, i32]
         L.orc_w_value.restype = ctypes.c_double
-        L.orc_layer.argtypes = [i64, i32, i32, i32, i32, i32, i32] + [vp] * 16 + [i32]
+        L.orc_layer.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32] + [vp] * 16 + [i32]
         L.orc_layer.restype = i64
         _LIB = L
     return _LIB
@@ -129,12 +129,14 @@ def w_value(fmt: int, wrow: np.ndarray, j: int) -> float:
     return float(lib().orc_w_value(fmt, _p(wrow), j))
 
 
-def swiglu_quant(gu: np.ndarray, n_ff: int):
+def swiglu_quant(gu: np.ndarray, n_ff: int, layout: int = 0):
+    """H = silu(gate)*up of GU rows, then q8.  layout 0: gate j at column j,
+    up j at n_ff + j ("split"); 1: gate j at 2j, up j at 2j + 1."""
     gu = _c(gu, np.float32).reshape(-1, 2 * n_ff)
     rows = gu.shape[0]
     hq = np.zeros((rows, n_ff), np.int8)
     dh = np.zeros((rows, n_ff // 32), np.float32)
-    lib().orc_swiglu_quant(rows, n_ff, _p(gu), _p(hq), _p(dh))
+    lib().orc_swiglu_quant(rows, n_ff, int(layout), _p(gu), _p(hq), _p(dh))
     return hq, dh
 
 
@@ -176,7 +178,8 @@ def layer(L, threads: int | None = None) -> dict:
         gu=np.zeros((max(R, 1), 2 * n_ff), np.float32),
         hq=np.zeros((max(R, 1), n_ff), np.int8), dh=np.zeros((max(R, 1), n_ff // 32), np.float32),
         dm=np.zeros((max(R, 1), d), np.float32), out=np.zeros((max(T, 1), d), np.float32))
-    bad = lib().orc_layer(T, d, n_ff, E, k, s.gu_fmt, s.down_fmt, _p(x), _p(ids), _p(w),
+    bad = lib().orc_layer(T, d, n_ff, E, k, s.gu_fmt, s.down_fmt, getattr(s, "gu_layout", 0),
+                          _p(x), _p(ids), _p(w),
                           _p(pack), _p(eoff), _p(o["counts"]), _p(o["offsets"]),
                           _p(o["row_src"]), _p(o["dst_of"]), _p(o["xq"]), _p(o["dx"]),
                           _p(o["gu"]), _p(o["hq"]), _p(o["dh"]), _p(o["dm"]), _p(o["out"]),

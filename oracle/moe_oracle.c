@@ -30,7 +30,13 @@
  *                 matters; "Strata #2145", Descricao: MAGIC C operand).
  *   swiglu_q   -- H = silu(g)*u with g the gate half and u the up half of a
  *                 GU row, then q8 of H per 32-value block; H never stored
- *                 ("Strata #3752", commit "swiglu_quant").
+ *                 ("Strata #3752", commit "swiglu_quant").  The gate/up
+ *                 rows are "split" (gate j at j, up j at n_ff + j) or
+ *                 "interleaved" (gate j at 2j, up j at 2j + 1): the commit's
+ *                 test runs both; it names the layouts without defining
+ *                 them, and these are the plain readings.  The GU row's
+ *                 columns follow the weight rows, so only this step sees
+ *                 the layout.
  *   combine    -- out[t] = sum over the token's top-k ranks r = 0..k-1, in
  *                 that order, of w[t,r]*Dm[row(t,r)] with one fma per rank
  *                 (the layer spec's tiny configuration).
@@ -198,21 +204,29 @@ void orc_expert_rows(int fmt, int K, int n_out, const uint8_t *wmat,
 }
 
 /* ------------------------------------------------------- swiglu + quant */
-static void orc_swiglu_quant_row(int n_ff, const float *gu, int8_t *hq,
-                                 float *dh, float *hbuf) {
+/* gate/up row layouts */
+#define ORC_GU_SPLIT 0
+#define ORC_GU_INTERLEAVED 1
+
+static void orc_swiglu_quant_row(int n_ff, int layout, const float *gu,
+                                 int8_t *hq, float *dh, float *hbuf) {
   for (int j = 0; j < n_ff; j++) {
     float g = gu[j];
     float u = gu[n_ff + j];
+    if (layout == ORC_GU_INTERLEAVED) {
+      g = gu[2 * j];
+      u = gu[2 * j + 1];
+    }
     hbuf[j] = (g / (1.0f + expf(-g))) * u;
   }
   orc_q8_row(n_ff, hbuf, hq, dh);
 }
 
-void orc_swiglu_quant(int64_t rows, int n_ff, const float *gu, int8_t *hq,
-                      float *dh) {
+void orc_swiglu_quant(int64_t rows, int n_ff, int layout, const float *gu,
+                      int8_t *hq, float *dh) {
   float *h = (float *)malloc(sizeof(float) * n_ff);
   for (int64_t r = 0; r < rows; r++)
-    orc_swiglu_quant_row(n_ff, gu + r * 2 * n_ff, hq + r * n_ff,
+    orc_swiglu_quant_row(n_ff, layout, gu + r * 2 * n_ff, hq + r * n_ff,
                          dh + r * (n_ff / 32), h);
   free(h);
 }
@@ -234,7 +248,7 @@ void orc_combine(int64_t T, int k, int d, const float *w, const int32_t *dst_of,
 
 /* ------------------------------------------------------------ full layer */
 typedef struct {
-  int d, n_ff, k, gu_fmt, down_fmt;
+  int d, n_ff, k, gu_fmt, down_fmt, gu_layout;
   const uint8_t *pack;
   const int64_t *eoff;
   const int32_t *ids, *row_src;
@@ -262,7 +276,7 @@ static void *orc_rows_worker(void *p) {
     float *dh = j->dh + r * (j->n_ff / 32);
     orc_product_row(j->gu_fmt, j->d, nff2, wgu, j->xq + t * j->d,
                     j->dx + t * (j->d / 32), gu);
-    orc_swiglu_quant_row(j->n_ff, gu, hq, dh, hbuf);
+    orc_swiglu_quant_row(j->n_ff, j->gu_layout, gu, hq, dh, hbuf);
     orc_product_row(j->down_fmt, j->n_ff, j->d, wdn, hq, dh, j->dm + r * j->d);
   }
   free(hbuf);
@@ -278,7 +292,7 @@ static void *orc_rows_worker(void *p) {
  * out-of-range expert ids.
  */
 int64_t orc_layer(int64_t T, int d, int n_ff, int E, int k, int gu_fmt,
-                  int down_fmt, const float *x, const int32_t *ids,
+                  int down_fmt, int gu_layout, const float *x, const int32_t *ids,
                   const float *w, const uint8_t *pack, const int64_t *eoff,
                   int32_t *counts, int32_t *offsets, int32_t *row_src,
                   int32_t *dst_of, int8_t *xq, float *dx, float *gu,
@@ -290,7 +304,7 @@ int64_t orc_layer(int64_t T, int d, int n_ff, int E, int k, int gu_fmt,
   pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * threads);
   orc_job *jobs = (orc_job *)malloc(sizeof(orc_job) * threads);
   for (int i = 0; i < threads; i++) {
-    orc_job j = {d, n_ff, k, gu_fmt, down_fmt, pack, eoff, ids, row_src,
+    orc_job j = {d, n_ff, k, gu_fmt, down_fmt, gu_layout, pack, eoff, ids, row_src,
                  xq, dx, gu, hq, dh, dm, R * i / threads, R * (i + 1) / threads};
     jobs[i] = j;
     pthread_create(&th[i], NULL, orc_rows_worker, &jobs[i]);

@@ -24,7 +24,10 @@ the formats but never lay out their bytes):
 
 A weight matrix [rows x K] is row-major: each row is its K/64 (W2) or K/32
 (W4NL) blocks back to back.  An expert's gate/up matrix holds the gate rows
-0..n_ff-1 then the up rows n_ff..2*n_ff-1 ("split" layout).  The weight pack
+0..n_ff-1 then the up rows n_ff..2*n_ff-1 ("split" layout), or gate row j
+at row 2j and up row j at row 2j+1 ("interleaved").  An interleaved layer
+draws the same blocks as the split layer of the same seed, with the gate/up
+rows permuted.  The weight pack
 is every expert's gate/up matrix then its down matrix, each start 16-byte
 aligned; ``expert_offsets[e] = (gate/up byte offset, down byte offset)``.
 """
@@ -35,6 +38,8 @@ import numpy as np
 
 W2 = 1
 W4NL = 2
+GU_SPLIT = 0
+GU_INTERLEAVED = 1
 
 # 4-bit non-linear table of the W4NL format (the layer spec's mixed-format
 # configuration lists these 16 integers).
@@ -54,6 +59,7 @@ class LayerShape:
     k: int
     gu_fmt: int = W2
     down_fmt: int = W2
+    gu_layout: int = GU_SPLIT
 
 
 def row_bytes(fmt: int, K: int) -> int:
@@ -171,8 +177,12 @@ def draw_weights(rng: np.random.Generator, shape: LayerShape):
     pack = np.zeros(total, dtype=np.uint8)
     n_gu = gu_bytes // BLOCK_BYTES
     n_dn = dn_bytes // BLOCK_BYTES
+    rb = row_bytes(shape.gu_fmt, shape.d)
     for e in range(shape.E):
-        pack[offs[e, 0]:offs[e, 0] + gu_bytes] = draw_blocks(rng, n_gu).reshape(-1)
+        gu = draw_blocks(rng, n_gu).reshape(2 * shape.n_ff, rb)
+        if shape.gu_layout == GU_INTERLEAVED:
+            gu = np.stack([gu[:shape.n_ff], gu[shape.n_ff:]], axis=1).reshape(2 * shape.n_ff, rb)
+        pack[offs[e, 0]:offs[e, 0] + gu_bytes] = gu.reshape(-1)
         pack[offs[e, 1]:offs[e, 1] + dn_bytes] = draw_blocks(rng, n_dn).reshape(-1)
     return pack, offs
 

@@ -314,7 +314,7 @@ def check_layer_consistency(layer=None):
         gu[m] = oracle.expert_rows(s.gu_fmt, s.d, 2 * s.n_ff, L.weight_pack[L.expert_offsets[e, 0]:],
                                    xq[tok[m]], dx[tok[m]])
     assert np.array_equal(o["gu"], gu)
-    hq, dh = oracle.swiglu_quant(gu, s.n_ff)
+    hq, dh = oracle.swiglu_quant(gu, s.n_ff, s.gu_layout)
     assert np.array_equal(o["hq"], hq) and np.array_equal(o["dh"], dh)
     dm = np.zeros((len(row_src), s.d), np.float32)
     for e in np.unique(exp):
@@ -326,9 +326,41 @@ def check_layer_consistency(layer=None):
     assert np.array_equal(o["out"], out)
 
 
+def check_interleaved_gate_up_is_a_permutation(seed=11):
+    """Interleaved gate/up rows (gate j at row 2j, up j at 2j+1) are the split
+    rows permuted: the same seed draws the same blocks, GU's columns follow
+    the weight rows, and swiglu_quant pairs gate j with up j either way, so
+    Hq, its scales, Dm and out are the split layer's bits.  Pins the
+    interleaved reading to the split path (itself pinned above): a gate/up
+    swap, or pairing gate j with another row, changes H."""
+    base = dict(T=37, d=256, n_ff=96, E=6, k=3, gu_fmt=synth.W2, down_fmt=synth.W4NL)
+    Ls = synth.make_layer(synth.LayerShape(**base), seed=seed, routing="topk", bias=True,
+                          outliers=True)
+    Li = synth.make_layer(synth.LayerShape(**base, gu_layout=synth.GU_INTERLEAVED), seed=seed,
+                          routing="topk", bias=True, outliers=True)
+    n_ff, rb = base["n_ff"], synth.row_bytes(synth.W2, base["d"])
+    perm = np.stack([np.arange(n_ff), n_ff + np.arange(n_ff)], axis=1).reshape(-1)
+    for e in range(base["E"]):
+        o0 = Ls.expert_offsets[e, 0]
+        ws = Ls.weight_pack[o0:o0 + 2 * n_ff * rb].reshape(2 * n_ff, rb)
+        wi = Li.weight_pack[o0:o0 + 2 * n_ff * rb].reshape(2 * n_ff, rb)
+        assert np.array_equal(wi, ws[perm]) and not np.array_equal(wi, ws)
+    os_, oi = oracle.layer(Ls, threads=2), oracle.layer(Li, threads=2)
+    assert np.array_equal(oi["gu"], os_["gu"][:, perm])
+    for key in ("hq", "dh", "dm", "out"):
+        assert np.array_equal(oi[key], os_[key]), key
+    hq, dh = oracle.swiglu_quant(os_["gu"][:, perm], n_ff, synth.GU_INTERLEAVED)
+    assert np.array_equal(hq, os_["hq"]) and np.array_equal(dh, os_["dh"])
+    # the gate half is not the up half: reading the split row as interleaved
+    # gives other bytes
+    hq_wrong, _ = oracle.swiglu_quant(os_["gu"], n_ff, synth.GU_INTERLEAVED)
+    assert not np.array_equal(hq_wrong, os_["hq"])
+
+
 ALL_PINS = [
     check_route_golden, check_route_vs_argsort, check_route_bad_ids,
     check_q8_golden, check_q8_numpy_and_invariants, check_decode_golden,
     check_products_golden, check_block_sums, check_products_brute_force,
     check_swiglu_quant, check_combine, check_layer_vs_dense,
+    check_interleaved_gate_up_is_a_permutation,
 ]
