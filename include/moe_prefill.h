@@ -60,8 +60,13 @@ typedef struct CUstream_st *moe_stream_t; /* == cudaStream_t */
  * A weight matrix [rows x K] is row-major, each row its blocks back to back. */
 enum { MOE_FMT_W2 = 1, MOE_FMT_W4NL = 2 };
 
-/* Gate/up row order: gate rows 0..n_ff-1, then up rows n_ff..2*n_ff-1. */
-enum { MOE_GU_SPLIT = 0 };
+/* Row order of a gate/up matrix [2*n_ff x d] ("Strata #3752", commit
+ * "swiglu_quant": its test runs "split and interleaved gate/up rows"; the
+ * page names the two without defining them -- these are the plain readings):
+ *   MOE_GU_SPLIT        gate rows 0..n_ff-1, then up rows n_ff..2*n_ff-1
+ *   MOE_GU_INTERLEAVED  gate row j at row 2j, up row j at row 2j+1
+ * H = silu(gate)*up pairs gate j with up j either way. */
+enum { MOE_GU_SPLIT = 0, MOE_GU_INTERLEAVED = 1 };
 
 enum {
   MOE_OK = 0,
@@ -96,7 +101,7 @@ typedef struct MoeLayerDesc {
   int32_t k;        /* experts per token (top-k)                      */
   int32_t gu_fmt;   /* MOE_FMT_* of the gate/up matrices              */
   int32_t down_fmt; /* MOE_FMT_* of the down matrices                 */
-  int32_t gu_layout;/* MOE_GU_SPLIT                                   */
+  int32_t gu_layout;/* MOE_GU_SPLIT or MOE_GU_INTERLEAVED            */
   uint32_t flags;   /* must be 0                                      */
   int32_t reserved; /* must be 0                                      */
   int64_t weight_pack_bytes; /* size of the tiled weight pack; expert matrices must lie inside */
@@ -117,7 +122,9 @@ typedef struct MoeLayerDesc {
  *                            2i+1 holds value i+8
  *   dx      fp32  [R*sd]     q8 scales of x per routed row, rows padded to
  *                            sd = d/32 rounded up to a multiple of 4
- *   gu      fp32  [R*2*n_ff] gate/up rows (gate half, then up half)
+ *   gu      fp32  [R*2*n_ff] gate/up rows, columns in the weight rows' order:
+ *                            gate j at j and up j at n_ff+j (MOE_GU_SPLIT)
+ *                            or at 2j and 2j+1 (MOE_GU_INTERLEAVED)
  *   hq      fp16  [R*n_ff]   q8 values of H as exact fp16 integers, stored
  *                            pair-interleaved like xq
  *   dh      fp32  [R*sf]     q8 scales of H, rows padded to sf = n_ff/32
@@ -148,9 +155,10 @@ int moe_workspace_view(const MoeLayerDesc *desc, void *workspace,
  * bpr = K / (values per block) blocks per row:
  *   tile t holds NW = min(256, N_out - 256t) rows and starts at byte
  *     256*t*bpr*18 of the matrix.  Down: rows 256t .. 256t+NW-1.  Gate/up:
- *     gate rows 128t .. 128t+NW/2-1, then up rows n_ff+128t ..
- *     n_ff+128t+NW/2-1 (tile row r < NW/2 is gate row 128t+r, tile row
- *     NW/2+r is up row n_ff+128t+r);
+ *     gate rows 128t .. 128t+NW/2-1, then the matching up rows (tile row
+ *     r < NW/2 is gate output 128t+r, tile row NW/2+r is up output
+ *     128t+r); gate output g is row g of the row-major matrix and up output
+ *     g row n_ff+g (MOE_GU_SPLIT), or rows 2g and 2g+1 (MOE_GU_INTERLEAVED);
  *   chunk c of a tile covers blocks 4c .. 4c+nbc-1, nbc = min(4, bpr - 4c),
  *     and starts at byte 4*c*NW*18 of the tile;
  *   inside a chunk, the 16 code bytes (block bytes 2..17) of (tile row r,

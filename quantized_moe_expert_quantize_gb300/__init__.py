@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(PKG, "libmoeprefill.so")
 MOE_FMT_W2 = 1
 MOE_FMT_W4NL = 2
 MOE_GU_SPLIT = 0
+MOE_GU_INTERLEAVED = 1
 
 MOE_OK = 0
 MOE_ERR_NULL = -1
@@ -136,8 +137,8 @@ def _check(rc: int, where: str):
 
 
 def make_desc(T, d, n_ff, E, k, gu_fmt=MOE_FMT_W2, down_fmt=MOE_FMT_W2,
-              weight_pack_bytes=0) -> MoeLayerDesc:
-    return MoeLayerDesc(T, d, n_ff, E, k, gu_fmt, down_fmt, MOE_GU_SPLIT, 0, 0,
+              weight_pack_bytes=0, gu_layout=MOE_GU_SPLIT) -> MoeLayerDesc:
+    return MoeLayerDesc(T, d, n_ff, E, k, gu_fmt, down_fmt, int(gu_layout), 0, 0,
                         int(weight_pack_bytes))
 
 
@@ -220,10 +221,11 @@ def moe_tile_weights(desc, weight_pack, expert_offsets, tiled_pack, tiled_offset
         "moe_tile_weights")
 
 
-def tile_weights(T, d, n_ff, E, k, gu_fmt, down_fmt, weight_pack, expert_offsets, stream=None):
+def tile_weights(T, d, n_ff, E, k, gu_fmt, down_fmt, weight_pack, expert_offsets, stream=None,
+                 gu_layout=MOE_GU_SPLIT):
     """Tile a device-resident row-major pack; returns (desc, tiled pack,
     tiled offsets), desc.weight_pack_bytes being the tiled pack's size."""
-    desc = make_desc(T, d, n_ff, E, k, gu_fmt, down_fmt, 0)
+    desc = make_desc(T, d, n_ff, E, k, gu_fmt, down_fmt, 0, gu_layout)
     desc.weight_pack_bytes = tiled_pack_bytes(desc)
     dev = weight_pack.device
     tiled = torch.empty(desc.weight_pack_bytes, dtype=torch.uint8, device=dev)

@@ -71,7 +71,7 @@ int validate_desc(const MoeLayerDesc* d) {
   if ((int64_t)d->T * d->k >= ((int64_t)1 << 24)) return MOE_ERR_SHAPE;
   if ((d->gu_fmt != MOE_FMT_W2 && d->gu_fmt != MOE_FMT_W4NL) ||
       (d->down_fmt != MOE_FMT_W2 && d->down_fmt != MOE_FMT_W4NL) ||
-      d->gu_layout != MOE_GU_SPLIT || d->flags != 0 || d->reserved != 0)
+      (d->gu_layout != MOE_GU_SPLIT && d->gu_layout != MOE_GU_INTERLEAVED) || d->flags != 0 || d->reserved != 0)
     return MOE_ERR_FORMAT;
   if (d->weight_pack_bytes < 0) return MOE_ERR_SHAPE;
   if (!tc_supported(*d)) return MOE_ERR_SHAPE;
@@ -187,6 +187,7 @@ int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaSt
   a.E = c.d.E;
   a.status = c.v.status;
   a.rows_max = rows_max(c.d);
+  a.gu_layout = c.d.gu_layout;
   if (which == 0) {
     a.act = (const __half*)c.v.xq;
     a.act_d = c.v.dx;
@@ -224,7 +225,7 @@ int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaSt
 
 int run_swiglu(Ctx& c, cudaStream_t st) {
   return launch_rc(launch_swiglu_quant(c.v.gu, c.v.offsets + c.d.E, rows_max(c.d), c.d.n_ff,
-                                       (__half*)c.v.hq, c.v.dh, st));
+                                       c.d.gu_layout, (__half*)c.v.hq, c.v.dh, st));
 }
 
 int run_combine(Ctx& c, const float* w, float* out, cudaStream_t st) {

@@ -68,9 +68,10 @@ cudaError_t launch_route(const int32_t* ids, int64_t n, int E, int32_t* hist,
 // d [rows_max x scale_stride(K)]
 cudaError_t launch_quant_q8(const float* x, int64_t T, int K, int k, const int32_t* dst_of,
                             int64_t rows_max, __half* q, float* d, cudaStream_t st);
-// swiglu + q8 of GU [rows x 2 n_ff]: hq [rows_max x n_ff], dh [rows_max x scale_stride(n_ff)]
+// swiglu + q8 of GU [rows x 2 n_ff] (gate/up columns in layout gu_layout):
+// hq [rows_max x n_ff], dh [rows_max x scale_stride(n_ff)]
 cudaError_t launch_swiglu_quant(const float* gu, const int32_t* nrows_dev, int64_t rows_max,
-                                int n_ff, __half* hq, float* dh, cudaStream_t st);
+                                int n_ff, int gu_layout, __half* hq, float* dh, cudaStream_t st);
 cudaError_t launch_combine(const float* topk_w, const int32_t* dst_of, const float* dm,
                            int64_t T, int k, int d, float* out, cudaStream_t st);
 
@@ -88,7 +89,9 @@ struct GemmArgs {
   const float* act_d;        // activation scales [rows_max x scale_stride(K)]
   int K;                     // reduction length
   int N_out;                 // output columns (weight rows)
-  float* out;                // [rows x N_out] (unused when hq is set)
+  float* out;                // [rows x N_out] (unused when hq is set); gate/up
+                             //   columns in layout gu_layout
+  int gu_layout;             // MOE_GU_*
   __half* hq;                // gate/up only: if set, swiglu_quant is fused and Hq / dh
   float* dh;                 //   are written instead of GU
   int64_t rows_max;          // capacity of the routed-row buffers (T*k)

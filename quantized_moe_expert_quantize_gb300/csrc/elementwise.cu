@@ -94,7 +94,8 @@ quant_q8_kernel(const float* __restrict__ x, int64_t groups, int K, int k,
 
 __global__ void __launch_bounds__(256)
 swiglu_quant_kernel(const float* __restrict__ gu, const int32_t* __restrict__ nrows_dev,
-                    int64_t rows_max, int n_ff, __half* __restrict__ hq, float* __restrict__ dh) {
+                    int64_t rows_max, int n_ff, int gu_layout, __half* __restrict__ hq,
+                    float* __restrict__ dh) {
   const int per_row = n_ff / 8;
   // rows actually routed, clamped to the buffers (a stale count cannot overrun)
   const int64_t nrows = min((int64_t)max(*nrows_dev, 0), rows_max);
@@ -105,11 +106,27 @@ swiglu_quant_kernel(const float* __restrict__ gu, const int32_t* __restrict__ nr
   if (ok) {
     const int64_t row = g / per_row;
     const int c = (int)(g - row * per_row);
-    const float4* gp = reinterpret_cast<const float4*>(gu + row * 2 * n_ff + c * 8);
-    const float4* up = reinterpret_cast<const float4*>(gu + row * 2 * n_ff + n_ff + c * 8);
-    const float4 g0 = __ldcs(gp), g1 = __ldcs(gp + 1), u0 = __ldcs(up), u1 = __ldcs(up + 1);
-    const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-    const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    float gv[8], uv[8];
+    if (gu_layout == MOE_GU_INTERLEAVED) {
+      // outputs 8c..8c+7: gate j at column 2j, up j at 2j+1
+      const float4* p = reinterpret_cast<const float4*>(gu + row * 2 * n_ff + c * 16);
+#pragma unroll
+      for (int q = 0; q < 4; q++) {
+        const float4 f = __ldcs(p + q);
+        gv[2 * q] = f.x;
+        uv[2 * q] = f.y;
+        gv[2 * q + 1] = f.z;
+        uv[2 * q + 1] = f.w;
+      }
+    } else {
+      const float4* gp = reinterpret_cast<const float4*>(gu + row * 2 * n_ff + c * 8);
+      const float4* up = reinterpret_cast<const float4*>(gu + row * 2 * n_ff + n_ff + c * 8);
+      const float4 g0 = __ldcs(gp), g1 = __ldcs(gp + 1), u0 = __ldcs(up), u1 = __ldcs(up + 1);
+      gv[0] = g0.x; gv[1] = g0.y; gv[2] = g0.z; gv[3] = g0.w;
+      gv[4] = g1.x; gv[5] = g1.y; gv[6] = g1.z; gv[7] = g1.w;
+      uv[0] = u0.x; uv[1] = u0.y; uv[2] = u0.z; uv[3] = u0.w;
+      uv[4] = u1.x; uv[5] = u1.y; uv[6] = u1.z; uv[7] = u1.w;
+    }
 #pragma unroll
     for (int i = 0; i < 8; i++) {
       // silu(g) * u = (g / (1 + exp(-g))) * u, each step rounded to fp32
@@ -172,11 +189,11 @@ cudaError_t launch_quant_q8(const float* x, int64_t T, int K, int k, const int32
 }
 
 cudaError_t launch_swiglu_quant(const float* gu, const int32_t* nrows_dev, int64_t rows_max,
-                                int n_ff, __half* hq, float* dh, cudaStream_t st) {
+                                int n_ff, int gu_layout, __half* hq, float* dh, cudaStream_t st) {
   const int64_t groups = rows_max * (n_ff / 8);
   if (groups == 0) return cudaSuccess;
   swiglu_quant_kernel<<<blocks_for(groups, 256), 256, 0, st>>>(gu, nrows_dev, rows_max, n_ff,
-                                                                hq, dh);
+                                                                gu_layout, hq, dh);
   count_launch();
   return cudaGetLastError();
 }

@@ -79,6 +79,7 @@ struct SmArgs {
   int E;
   int K, N_out, bpr;
   float* out;
+  int gu_layout;
   __half* hq;
   float* dh;
   int64_t rows_max;
@@ -433,17 +434,25 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
       } else if (MODE == kModeGU) {
         if (!active) continue;
         const int n_ff = a.N_out >> 1;
-        // gate and up outputs 128t + 16w + g (+8)
+        // gate and up outputs 128t + 16w + g (+8): columns o and n_ff + o
+        // (split), or 2o and 2o + 1 (interleaved)
         const int o = wt * (kTN / 2) + 16 * warp + g;
+        const bool inter = a.gu_layout == MOE_GU_INTERLEAVED;
 #pragma unroll
         for (int nt = 0; nt < 4; nt++)
 #pragma unroll
           for (int i = 0; i < 4; i++) {
             const int rr = 8 * nt + 2 * cq + (i & 1);
             if (rr < u) {
-              float* orow = a.out + (int64_t)(t.y + rr) * a.N_out + o + 8 * (i >> 1);
-              orow[0] = acc[0][nt][i];
-              orow[n_ff] = acc[1][nt][i];
+              const int oo = o + 8 * (i >> 1);
+              float* orow = a.out + (int64_t)(t.y + rr) * a.N_out;
+              if (inter) {
+                *reinterpret_cast<float2*>(orow + 2 * oo) =
+                    make_float2(acc[0][nt][i], acc[1][nt][i]);
+              } else {
+                orow[oo] = acc[0][nt][i];
+                orow[n_ff + oo] = acc[1][nt][i];
+              }
             }
           }
       } else {
@@ -569,6 +578,7 @@ cudaError_t launch_gemm_small(const GemmArgs& g, cudaStream_t st) {
   a.N_out = g.N_out;
   a.bpr = g.K / block_values(g.fmt);
   a.out = g.out;
+  a.gu_layout = g.gu_layout;
   a.hq = g.hq;
   a.dh = g.dh;
   a.rows_max = g.rows_max;

@@ -141,7 +141,8 @@ struct TcArgs {
   int K;
   int N_out;
   int bpr;              // weight blocks per row
-  float* out;           // GU [rows x N_out] or Dm [rows x N_out]
+  float* out;           // GU [rows x N_out] (gate/up columns in layout gu_layout) or Dm
+  int gu_layout;        // MOE_GU_*
   __half* hq;           // fused swiglu_quant: Hq [rows x N_out/2], pair-interleaved
   float* dh;            // fused swiglu_quant: scales [rows x scale_stride(N_out/2)]
   int64_t rows_max;
@@ -479,12 +480,25 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
       } else if (MODE == kModeGU) {
         // gate outputs 128t + 32h .. + 31, and the matching up outputs
         const int o = (I.o0 >> 1) + 32 * h;
-        float* gp = a.out + row * a.N_out + o;
-        float* up = gp + (a.N_out >> 1);
+        if (a.gu_layout == MOE_GU_INTERLEAVED) {
+          // gate j at column 2j, up j at 2j+1: 8 floats = outputs 4m .. 4m+3
+          float* p = a.out + row * a.N_out + 2 * o;
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-          st_global_v8(gp + 8 * j, acc + 4 * j);
-          st_global_v8(up + 8 * j, acc + 16 + 4 * j);
+          for (int m = 0; m < 8; m++) {
+            const float2 g0 = acc[2 * m], g1 = acc[2 * m + 1];
+            const float2 u0 = acc[16 + 2 * m], u1 = acc[16 + 2 * m + 1];
+            const float2 v[4] = {make_float2(g0.x, u0.x), make_float2(g0.y, u0.y),
+                                 make_float2(g1.x, u1.x), make_float2(g1.y, u1.y)};
+            st_global_v8(p + 8 * m, v);
+          }
+        } else {
+          float* gp = a.out + row * a.N_out + o;
+          float* up = gp + (a.N_out >> 1);
+#pragma unroll
+          for (int j = 0; j < 4; j++) {
+            st_global_v8(gp + 8 * j, acc + 4 * j);
+            st_global_v8(up + 8 * j, acc + 16 + 4 * j);
+          }
         }
       } else {
         // swiglu_quant fused: H = silu(g) * u for the 32 outputs
@@ -753,6 +767,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
   a.out = g.out;
   a.hq = g.hq;
   a.dh = g.dh;
+  a.gu_layout = g.gu_layout;
   a.rows_max = g.rows_max;
   a.status = g.status;
 

@@ -6,7 +6,9 @@
 //   tile t holds NW = min(256, N_out - 256t) rows, at byte 256 * t * bpr * 18:
 //     down: rows 256t .. 256t+NW-1;
 //     gate/up: gate rows 128t .. 128t+NW/2-1, then the up rows
-//     n_ff+128t .. n_ff+128t+NW/2-1 (a tile yields whole blocks of H);
+//     n_ff+128t .. n_ff+128t+NW/2-1 (a tile yields whole blocks of H) --
+//     gate row g is row g of the source matrix and up row g is row n_ff+g
+//     (split layout), or rows 2g and 2g+1 (interleaved layout);
 //   chunk c of a tile covers blocks 4c .. 4c+nbc-1, nbc = min(4, bpr - 4c),
 //     at byte 4 * c * NW * 18 of the tile;
 //   inside a chunk: the 16 code bytes of (row r, block j) at (j*NW + r)*16,
@@ -28,6 +30,7 @@ struct TileJob {
   int64_t* dst_eoff;        // [E][2]
   int32_t* status;          // may be null
   int E;
+  int gu_layout;            // MOE_GU_*
   int N[2], K[2], bpr[2];
   int64_t mbytes[2];        // bytes of one matrix
 };
@@ -56,9 +59,11 @@ __global__ void tile_weights_kernel(const TileJob j) {
     } else {
       // gate/up: tile t pairs gate rows 128t.. with the up rows n_ff + 128t..
       const int n_ff = j.N[0] >> 1;
-      const int gr = row < n_ff ? row : row - n_ff;
+      const bool inter = j.gu_layout == MOE_GU_INTERLEAVED;
+      const bool up = inter ? (row & 1) : row >= n_ff;
+      const int gr = inter ? row >> 1 : (up ? row - n_ff : row);  // gate/up output
       t = gr >> 7;
-      r = (gr & 127) + (row < n_ff ? 0 : min(128, n_ff - 128 * t));
+      r = (gr & 127) + (up ? min(128, n_ff - 128 * t) : 0);
     }
     const int nw = min(256, j.N[which] - 256 * t);
     const int c = blk >> 2, jj = blk & 3, nbc = min(4, bpr - 4 * c);
@@ -104,6 +109,7 @@ cudaError_t launch_tile_weights(const MoeLayerDesc& d, const uint8_t* src, int64
   j.dst_eoff = dst_eoff;
   j.status = status;
   j.E = d.E;
+  j.gu_layout = d.gu_layout;
   j.N[0] = 2 * d.n_ff;
   j.K[0] = d.d;
   j.N[1] = d.d;

@@ -73,7 +73,7 @@ class DeviceLayer:
         # row-major pack as drawn, then the tiled pack the layer reads
         self.raw_pack = torch.from_numpy(L.weight_pack).to(dev)
         self.raw_eoff = torch.from_numpy(L.expert_offsets).to(dev)
-        self.desc = M.make_desc(s.T, s.d, s.n_ff, s.E, s.k, s.gu_fmt, s.down_fmt, 0)
+        self.desc = M.make_desc(s.T, s.d, s.n_ff, s.E, s.k, s.gu_fmt, s.down_fmt, 0, s.gu_layout)
         self.desc.weight_pack_bytes = M.tiled_pack_bytes(self.desc)
         self.pack = torch.full((self.desc.weight_pack_bytes,), 0xA5, dtype=torch.uint8, device=dev)
         self.eoff = torch.full((s.E, 2), -1, dtype=torch.int64, device=dev)
@@ -201,7 +201,7 @@ def oracle_rows(L: synth.Layer, o_route: dict, xq, dx, rows: np.ndarray):
         gu[i] = oracle.expert_rows(s.gu_fmt, s.d, 2 * s.n_ff,
                                    L.weight_pack[L.expert_offsets[e, 0]:],
                                    xq[tok[i]][None], dx[tok[i]][None])[0]
-    hq, dh = oracle.swiglu_quant(gu, s.n_ff)
+    hq, dh = oracle.swiglu_quant(gu, s.n_ff, s.gu_layout)
     for i in range(len(rows)):
         e = int(exp[i])
         dm[i] = oracle.expert_rows(s.down_fmt, s.n_ff, s.d,

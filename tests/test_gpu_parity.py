@@ -33,6 +33,13 @@ SMALL = {
                                               seed=9, routing="topk", bias=False, outliers=True),
     "flat_w2_w4nl": lambda: synth.make_layer(synth.LayerShape(128, 256, 128, 16, 4, synth.W2, synth.W4NL),
                                              seed=10, routing="flat", outliers=True),
+    # interleaved gate/up rows (gate j at row 2j, up j at 2j+1)
+    "mid_w2_w2_inter": lambda: synth.make_layer(
+        synth.LayerShape(300, 512, 192, 16, 4, synth.W2, synth.W2, synth.GU_INTERLEAVED),
+        seed=7, routing="topk", bias=True, outliers=True),
+    "mid_w4nl_w2_inter": lambda: synth.make_layer(
+        synth.LayerShape(257, 384, 128, 12, 3, synth.W4NL, synth.W2, synth.GU_INTERLEAVED),
+        seed=8, routing="topk", bias=True, outliers=True),
 }
 
 
@@ -73,7 +80,27 @@ def test_layer_replays_from_a_cuda_graph(M):
     assert not torch.equal(got, ref)
 
 
-@pytest.mark.parametrize("name", ["mid_w2_w2", "mid_w2_w4nl", "mid_w4nl_w4nl", "flat_w2_w4nl"])
+def test_interleaved_gate_up_equals_split(M):
+    """The same layer with its gate/up rows interleaved instead of split
+    gives the same Hq, Dm and out bits on the GPU, and GU permuted."""
+    Ls = SMALL["mid_w2_w2"]()
+    Li = SMALL["mid_w2_w2_inter"]()
+    a, b = DeviceLayer(M, Ls), DeviceLayer(M, Li)
+    for mode in ("layer", "stages"):
+        for dl in (a, b):
+            dl.run_layer() if mode == "layer" else dl.run_stages()
+            assert dl.status() == 0
+        R = int(a.get("offsets")[-1])
+        for key in ("hq", "dh", "dm"):
+            assert np.array_equal(a.get(key, R), b.get(key, R)), (mode, key)
+        assert torch.equal(a.out, b.out), mode
+    n_ff = Ls.shape.n_ff
+    perm = np.stack([np.arange(n_ff), n_ff + np.arange(n_ff)], axis=1).reshape(-1)
+    assert np.array_equal(b.get("gu", R), a.get("gu", R)[:, perm])
+
+
+@pytest.mark.parametrize("name", ["mid_w2_w2", "mid_w2_w4nl", "mid_w4nl_w4nl", "flat_w2_w4nl",
+                                  "mid_w2_w2_inter"])
 def test_fused_swiglu_equals_stages(M, name):
     """The layer's gate/up epilogue with swiglu_quant fused writes the same Hq
     and dh bits as the gate/up stage followed by the swiglu_quant stage."""
@@ -293,18 +320,22 @@ def test_bad_expert_offset_is_skipped_and_flagged(M):
     assert dl.status() & M.MOE_STATUS_BAD_OFFSET
 
 
-def _tile_reference(pack, eoff, fmt_gu, fmt_dn, d, n_ff, E):
+def _tile_reference(pack, eoff, fmt_gu, fmt_dn, d, n_ff, E, gu_layout=synth.GU_SPLIT):
     """The tiled layout of the C header, written out with numpy."""
     out = []
     for e in range(E):
         for which, (fmt, N, K) in enumerate(((fmt_gu, 2 * n_ff, d), (fmt_dn, d, n_ff))):
             bpr = K // synth.BLOCK_VALUES[fmt]
             m = pack[eoff[e, which]:eoff[e, which] + N * bpr * 18].reshape(N, bpr, 18)
+            if which == 0 and gu_layout == synth.GU_INTERLEAVED:
+                gate, up = m[0::2], m[1::2]
+            else:
+                gate, up = m[:n_ff], m[n_ff:]
             for t in range(0, N, 256):
                 nw = min(256, N - t)
                 if which == 0:   # gate rows t/2 .., then the matching up rows
                     g0 = t // 2
-                    rows = np.concatenate([m[g0:g0 + nw // 2], m[n_ff + g0:n_ff + g0 + nw // 2]])
+                    rows = np.concatenate([gate[g0:g0 + nw // 2], up[g0:g0 + nw // 2]])
                 else:
                     rows = m[t:t + nw]
                 for c in range(0, bpr, 4):
@@ -315,7 +346,9 @@ def _tile_reference(pack, eoff, fmt_gu, fmt_dn, d, n_ff, E):
 
 
 @pytest.mark.parametrize("shape", [synth.LayerShape(8, 384, 192, 3, 2, synth.W2, synth.W4NL),
-                                   synth.LayerShape(8, 640, 320, 2, 1, synth.W4NL, synth.W2)])
+                                   synth.LayerShape(8, 640, 320, 2, 1, synth.W4NL, synth.W2),
+                                   synth.LayerShape(8, 384, 192, 3, 2, synth.W2, synth.W2,
+                                                    synth.GU_INTERLEAVED)])
 def test_tiled_pack_layout(M, shape):
     """moe_tile_weights writes exactly the documented byte permutation, with
     ragged last tiles (N_out % 256 == 128) and ragged last chunks."""
@@ -324,7 +357,7 @@ def test_tiled_pack_layout(M, shape):
     torch.cuda.synchronize()
     assert int(dl.tile_status.item()) == 0
     ref = _tile_reference(L.weight_pack, L.expert_offsets, shape.gu_fmt, shape.down_fmt,
-                          shape.d, shape.n_ff, shape.E)
+                          shape.d, shape.n_ff, shape.E, shape.gu_layout)
     got = dl.pack.cpu().numpy()
     assert got.size == ref.size
     assert np.array_equal(got, ref)
