@@ -43,7 +43,10 @@
  *
  * Weight formats: see the byte layouts in the `synth` module (W2: 64-value
  * blocks, fp16 d, 2-bit codes c, value d*(c-2); W4NL: 32-value blocks, fp16
- * d, 4-bit index into a 16-entry table, value d*T[idx]).
+ * d, 4-bit index into a 16-entry table, value d*T[idx]; Q8_0: 32-value
+ * blocks of 34 bytes, fp16 d then 32 int8 codes q, value d*q -- the pages
+ * name Q8_0 as a down type of the swiglu_quant test ("Strata #3752") without
+ * laying it out, and this is the common layout of that name).
  */
 #include <math.h>
 #include <pthread.h>
@@ -53,7 +56,7 @@
 
 #define ORC_W2 1
 #define ORC_W4NL 2
-#define ORC_BLOCK_BYTES 18
+#define ORC_Q8_0 3
 
 static const int ORC_NL4[16] = {-127, -104, -83, -65, -49, -35, -22, -10,
                                 1,    13,   25,  38,  53,  69,  89,  113};
@@ -74,16 +77,18 @@ static float orc_half(uint16_t h) {
 }
 
 static int orc_block_values(int fmt) { return fmt == ORC_W2 ? 64 : 32; }
+static int orc_block_bytes(int fmt) { return fmt == ORC_Q8_0 ? 34 : 18; }
 
 int64_t orc_row_bytes(int fmt, int K) {
-  return (int64_t)(K / orc_block_values(fmt)) * ORC_BLOCK_BYTES;
+  return (int64_t)(K / orc_block_values(fmt)) * orc_block_bytes(fmt);
 }
 
-/* Integer weight value (c-2 or T[idx]) of element j of a row. */
+/* Integer weight value (c-2, T[idx] or q) of element j of a row. */
 static int orc_w_int(int fmt, const uint8_t *row, int j) {
   int bv = orc_block_values(fmt);
-  const uint8_t *blk = row + (int64_t)(j / bv) * ORC_BLOCK_BYTES;
+  const uint8_t *blk = row + (int64_t)(j / bv) * orc_block_bytes(fmt);
   int jj = j % bv;
+  if (fmt == ORC_Q8_0) return (int)(int8_t)blk[2 + jj];
   if (fmt == ORC_W2) {
     int c = (blk[2 + jj / 4] >> (2 * (jj % 4))) & 3;
     return c - 2;
@@ -95,7 +100,7 @@ static int orc_w_int(int fmt, const uint8_t *row, int j) {
 /* fp16 scale of the block holding element j of a row, as fp32. */
 static float orc_w_scale(int fmt, const uint8_t *row, int j) {
   int bv = orc_block_values(fmt);
-  const uint8_t *blk = row + (int64_t)(j / bv) * ORC_BLOCK_BYTES;
+  const uint8_t *blk = row + (int64_t)(j / bv) * orc_block_bytes(fmt);
   return orc_half((uint16_t)(blk[0] | (blk[1] << 8)));
 }
 

@@ -21,6 +21,10 @@ the formats but never lay out their bytes):
 * W4NL -- 32 values per block, 18 bytes: fp16 ``d`` in bytes 0-1, then 16
   bytes of 4-bit indices.  Index ``j`` (0..31) sits in byte ``2 + j // 2``,
   low nibble for even ``j``.  Value = d * NL4_TABLE[index].
+* Q8_0 -- 32 values per block, 34 bytes: fp16 ``d`` in bytes 0-1, then the 32
+  int8 codes ``q_j`` in bytes 2..33.  Value = d * q_j.  (The pages name the
+  type without laying it out; this is the common layout of that name.)
+  Drawn codes lie in [-127, 127].
 
 A weight matrix [rows x K] is row-major: each row is its K/64 (W2) or K/32
 (W4NL) blocks back to back.  An expert's gate/up matrix holds the gate rows
@@ -38,6 +42,7 @@ import numpy as np
 
 W2 = 1
 W4NL = 2
+Q8_0 = 3
 GU_SPLIT = 0
 GU_INTERLEAVED = 1
 
@@ -46,8 +51,9 @@ GU_INTERLEAVED = 1
 NL4_TABLE = np.array([-127, -104, -83, -65, -49, -35, -22, -10,
                       1, 13, 25, 38, 53, 69, 89, 113], dtype=np.int8)
 
-BLOCK_BYTES = 18
-BLOCK_VALUES = {W2: 64, W4NL: 32}
+BLOCK_BYTES = 18                       # W2 and W4NL
+BLOCK_BYTES_OF = {W2: 18, W4NL: 18, Q8_0: 34}
+BLOCK_VALUES = {W2: 64, W4NL: 32, Q8_0: 32}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -64,7 +70,7 @@ class LayerShape:
 
 def row_bytes(fmt: int, K: int) -> int:
     """Bytes of one weight row of K values in format ``fmt``."""
-    return (K // BLOCK_VALUES[fmt]) * BLOCK_BYTES
+    return (K // BLOCK_VALUES[fmt]) * BLOCK_BYTES_OF[fmt]
 
 
 def _align16(n: int) -> int:
@@ -146,15 +152,20 @@ def draw_flat_routing(rng: np.random.Generator, T: int, E: int, k: int):
     return ids.astype(np.int32), w
 
 
-def draw_blocks(rng: np.random.Generator, n_blocks: int) -> np.ndarray:
-    """n_blocks random 18-byte blocks: fp16 d = 0.02*U(0.5,1.5), random codes.
-
-    Uniform code bytes give uniform 2-bit codes and uniform 4-bit indices.
+def draw_blocks(rng: np.random.Generator, n_blocks: int, fmt: int = W2) -> np.ndarray:
+    """n_blocks random blocks of format ``fmt``: fp16 d = 0.02*U(0.5,1.5),
+    random codes.  Uniform code bytes give uniform 2-bit codes and uniform
+    4-bit indices (W2 and W4NL share the 18-byte draw); Q8_0 codes are
+    uniform in [-127, 127].
     """
     d = (0.02 * rng.uniform(0.5, 1.5, n_blocks)).astype(np.float16)
-    blocks = np.empty((n_blocks, BLOCK_BYTES), dtype=np.uint8)
+    blocks = np.empty((n_blocks, BLOCK_BYTES_OF[fmt]), dtype=np.uint8)
     blocks[:, 0:2] = d.view(np.uint8).reshape(n_blocks, 2)
-    blocks[:, 2:] = rng.integers(0, 256, size=(n_blocks, 16), dtype=np.uint8)
+    if fmt == Q8_0:
+        q = rng.integers(-127, 128, size=(n_blocks, 32)).astype(np.int8)
+        blocks[:, 2:] = q.view(np.uint8)
+    else:
+        blocks[:, 2:] = rng.integers(0, 256, size=(n_blocks, 16), dtype=np.uint8)
     return blocks
 
 
@@ -175,15 +186,15 @@ def pack_layout(shape: LayerShape):
 def draw_weights(rng: np.random.Generator, shape: LayerShape):
     offs, total, gu_bytes, dn_bytes = pack_layout(shape)
     pack = np.zeros(total, dtype=np.uint8)
-    n_gu = gu_bytes // BLOCK_BYTES
-    n_dn = dn_bytes // BLOCK_BYTES
+    n_gu = gu_bytes // BLOCK_BYTES_OF[shape.gu_fmt]
+    n_dn = dn_bytes // BLOCK_BYTES_OF[shape.down_fmt]
     rb = row_bytes(shape.gu_fmt, shape.d)
     for e in range(shape.E):
-        gu = draw_blocks(rng, n_gu).reshape(2 * shape.n_ff, rb)
+        gu = draw_blocks(rng, n_gu, shape.gu_fmt).reshape(2 * shape.n_ff, rb)
         if shape.gu_layout == GU_INTERLEAVED:
             gu = np.stack([gu[:shape.n_ff], gu[shape.n_ff:]], axis=1).reshape(2 * shape.n_ff, rb)
         pack[offs[e, 0]:offs[e, 0] + gu_bytes] = gu.reshape(-1)
-        pack[offs[e, 1]:offs[e, 1] + dn_bytes] = draw_blocks(rng, n_dn).reshape(-1)
+        pack[offs[e, 1]:offs[e, 1] + dn_bytes] = draw_blocks(rng, n_dn, shape.down_fmt).reshape(-1)
     return pack, offs
 
 

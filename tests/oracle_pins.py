@@ -38,11 +38,14 @@ def _fill(spec, n=32, dtype=np.float32):
 def np_decode_matrix(fmt: int, wmat: np.ndarray, rows: int, K: int):
     """Return (int values [rows, K], fp32 scales per value [rows, K])."""
     bv = synth.BLOCK_VALUES[fmt]
+    bb = synth.BLOCK_BYTES_OF[fmt]
     nb = K // bv
-    blk = wmat[: rows * nb * 18].reshape(rows, nb, 18)
+    blk = wmat[: rows * nb * bb].reshape(rows, nb, bb)
     d = blk[:, :, 0:2].copy().view(np.float16)[:, :, 0].astype(np.float32)
     codes = blk[:, :, 2:]
-    if fmt == synth.W2:
+    if fmt == synth.Q8_0:
+        ints = codes.copy().view(np.int8).astype(np.int32)
+    elif fmt == synth.W2:
         shifts = np.array([0, 2, 4, 6], dtype=np.uint8)
         c = (codes[:, :, :, None] >> shifts) & 3          # [rows, nb, 16, 4]
         ints = c.reshape(rows, nb, 64).astype(np.int32) - 2
@@ -174,9 +177,10 @@ def check_products_golden():
 
 def check_block_sums(seed=2):
     rng = np.random.default_rng(seed)
-    for fmt, K, bound in ((synth.W2, 256, 32 * 2 * 127), (synth.W4NL, 256, 32 * 127 * 127)):
+    for fmt, K, bound in ((synth.W2, 256, 32 * 2 * 127), (synth.W4NL, 256, 32 * 127 * 127),
+                          (synth.Q8_0, 256, 32 * 127 * 127)):
         nb = K // synth.BLOCK_VALUES[fmt]
-        row = synth.draw_blocks(rng, nb).reshape(-1)
+        row = synth.draw_blocks(rng, nb, fmt).reshape(-1)
         q = rng.integers(-127, 128, K).astype(np.int8)
         s = oracle.block_sums(fmt, K, row, q)
         ints, _ = np_decode_matrix(fmt, row, 1, K)
@@ -190,9 +194,15 @@ def check_block_sums(seed=2):
             qe = np.full(K, -127, np.int8)
             s2 = oracle.block_sums(fmt, K, row2.reshape(-1), qe)
             assert np.all(s2 == 32 * 2 * 127)
-        else:
+        elif fmt == synth.W4NL:
             row2 = row.copy().reshape(nb, 18)
             row2[:, 2:] = 0                         # index 0 -> -127
+            qe = np.full(K, -127, np.int8)
+            s2 = oracle.block_sums(fmt, K, row2.reshape(-1), qe)
+            assert np.all(s2 == 32 * 127 * 127)
+        else:
+            row2 = row.copy().reshape(nb, 34)
+            row2[:, 2:] = 0x81                      # every code -127
             qe = np.full(K, -127, np.int8)
             s2 = oracle.block_sums(fmt, K, row2.reshape(-1), qe)
             assert np.all(s2 == 32 * 127 * 127)
@@ -202,9 +212,10 @@ def check_products_brute_force(seed=3):
     """Oracle products vs a float64 dot of the dequantized values."""
     rng = np.random.default_rng(seed)
     for fmt, K, n_out, rows in ((synth.W2, 256, 128, 16), (synth.W4NL, 640, 64, 8),
-                                (synth.W2, 2560, 32, 4), (synth.W2, 640, 64, 8)):
+                                (synth.W2, 2560, 32, 4), (synth.W2, 640, 64, 8),
+                                (synth.Q8_0, 640, 64, 8), (synth.Q8_0, 256, 32, 4)):
         nb = n_out * K // synth.BLOCK_VALUES[fmt]
-        wmat = synth.draw_blocks(rng, nb).reshape(-1)
+        wmat = synth.draw_blocks(rng, nb, fmt).reshape(-1)
         x = rng.standard_normal((rows, K)).astype(np.float32)
         x[0, 5] *= 30
         q, dq = oracle.quant_q8(x)
@@ -297,6 +308,15 @@ def check_layer_vs_dense(layer=None):
     return rel
 
 
+def check_q8_0_down_layer_vs_dense():
+    """A layer whose down matrices are Q8_0, against the dense float64 layer
+    (the same sanity band), and stage by stage."""
+    L = synth.make_layer(synth.LayerShape(24, 256, 64, 6, 2, synth.W2, synth.Q8_0), seed=13,
+                         routing="topk", bias=True)
+    check_layer_vs_dense(L)
+    check_layer_consistency(L)
+
+
 def check_layer_consistency(layer=None):
     """The layer entry point equals its stages run one by one."""
     L = layer or synth.config_layer(0)
@@ -362,5 +382,5 @@ ALL_PINS = [
     check_q8_golden, check_q8_numpy_and_invariants, check_decode_golden,
     check_products_golden, check_block_sums, check_products_brute_force,
     check_swiglu_quant, check_combine, check_layer_vs_dense,
-    check_interleaved_gate_up_is_a_permutation,
+    check_interleaved_gate_up_is_a_permutation, check_q8_0_down_layer_vs_dense,
 ]

@@ -16,6 +16,8 @@ MUTANTS = [
     ("w2_code_offset", "return c - 2;", "return c - 1;"),
     ("w2_bit_order", "(2 * (jj % 4))", "(2 * (3 - jj % 4))"),
     ("w4nl_nibble_order", "(4 * (jj % 2))", "(4 * (1 - jj % 2))"),
+    ("q8_0_unsigned_codes", "return (int)(int8_t)blk[2 + jj];", "return (int)blk[2 + jj];"),
+    ("q8_0_block_bytes", "return fmt == ORC_Q8_0 ? 34 : 18;", "return fmt == ORC_Q8_0 ? 33 : 18;"),
     ("half_exponent_bias", "ex - 25", "ex - 24"),
     ("dropped_last_block", "for (int b = 0; b < nb; b++) {\n      int32_t isum",
      "for (int b = 0; b < nb - 1; b++) {\n      int32_t isum"),
