@@ -57,8 +57,13 @@ typedef struct CUstream_st *moe_stream_t; /* == cudaStream_t */
  *               indices; index j sits in byte 2 + j/2, low nibble for even j.
  *               Value = d*T[idx], T = {-127,-104,-83,-65,-49,-35,-22,-10,1,
  *               13,25,38,53,69,89,113}.
+ * MOE_FMT_Q8_0: 32 values per 34-byte block: fp16 d, then 32 int8 codes q;
+ *               code j sits in byte 2 + j.  Value = d*q.  ("Strata #3752",
+ *               commit "swiglu_quant", names Q8_0 as a down type of its test
+ *               without laying it out; this is the common layout of that
+ *               name.)
  * A weight matrix [rows x K] is row-major, each row its blocks back to back. */
-enum { MOE_FMT_W2 = 1, MOE_FMT_W4NL = 2 };
+enum { MOE_FMT_W2 = 1, MOE_FMT_W4NL = 2, MOE_FMT_Q8_0 = 3 };
 
 /* Row order of a gate/up matrix [2*n_ff x d] ("Strata #3752", commit
  * "swiglu_quant": its test runs "split and interleaved gate/up rows"; the

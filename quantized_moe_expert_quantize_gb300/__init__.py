@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(PKG, "libmoeprefill.so")
 
 MOE_FMT_W2 = 1
 MOE_FMT_W4NL = 2
+MOE_FMT_Q8_0 = 3
 MOE_GU_SPLIT = 0
 MOE_GU_INTERLEAVED = 1
 

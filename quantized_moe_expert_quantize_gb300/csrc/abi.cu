@@ -69,9 +69,10 @@ int validate_desc(const MoeLayerDesc* d) {
       d->k > d->E)
     return MOE_ERR_SHAPE;
   if ((int64_t)d->T * d->k >= ((int64_t)1 << 24)) return MOE_ERR_SHAPE;
-  if ((d->gu_fmt != MOE_FMT_W2 && d->gu_fmt != MOE_FMT_W4NL) ||
-      (d->down_fmt != MOE_FMT_W2 && d->down_fmt != MOE_FMT_W4NL) ||
-      (d->gu_layout != MOE_GU_SPLIT && d->gu_layout != MOE_GU_INTERLEAVED) || d->flags != 0 || d->reserved != 0)
+  auto fmt_ok = [](int f) { return f == MOE_FMT_W2 || f == MOE_FMT_W4NL || f == MOE_FMT_Q8_0; };
+  if (!fmt_ok(d->gu_fmt) || !fmt_ok(d->down_fmt) ||
+      (d->gu_layout != MOE_GU_SPLIT && d->gu_layout != MOE_GU_INTERLEAVED) || d->flags != 0 ||
+      d->reserved != 0)
     return MOE_ERR_FORMAT;
   if (d->weight_pack_bytes < 0) return MOE_ERR_SHAPE;
   if (!tc_supported(*d)) return MOE_ERR_SHAPE;

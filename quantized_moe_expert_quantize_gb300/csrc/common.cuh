@@ -11,17 +11,22 @@ namespace moe {
 
 // ---------------------------------------------------------------- formats
 constexpr int kBlockBytes = 18;       // W2 and W4NL blocks are 18 bytes
+constexpr int kQ8Bytes = 34;          // Q8_0 blocks: fp16 d + 32 int8 codes
 constexpr int kW2Values = 64;         // values per W2 block
-constexpr int kW4Values = 32;         // values per W4NL block
+constexpr int kW4Values = 32;         // values per W4NL (and Q8_0) block
 constexpr int kQBlock = 32;           // q8 block of activations
 
 // Row stride (in floats) of a q8 scale matrix [rows x K/32]: padded to a
 // multiple of 4 so every row starts 16-byte aligned (tensor-map rule).
 __host__ __device__ inline int scale_stride(int K) { return ((K / 32) + 3) & ~3; }
 
-__host__ __device__ inline int block_values(int fmt) { return fmt == MOE_FMT_W2 ? kW2Values : kW4Values; }
+__host__ __device__ constexpr int block_values(int fmt) { return fmt == MOE_FMT_W2 ? kW2Values : kW4Values; }
+__host__ __device__ constexpr int block_bytes(int fmt) { return fmt == MOE_FMT_Q8_0 ? kQ8Bytes : kBlockBytes; }
+__host__ __device__ constexpr int code_bytes(int fmt) { return block_bytes(fmt) - 2; }
+// Blocks per chunk of the tiled pack: a 256-row chunk stays within 18 KB.
+__host__ __device__ constexpr int chunk_blocks(int fmt) { return fmt == MOE_FMT_Q8_0 ? 2 : 4; }
 __host__ __device__ inline int64_t row_bytes(int fmt, int K) {
-  return (int64_t)(K / block_values(fmt)) * kBlockBytes;
+  return (int64_t)(K / block_values(fmt)) * block_bytes(fmt);
 }
 
 // fp16 bit patterns of the integers -2..1 (W2 codes 0..3 minus 2).

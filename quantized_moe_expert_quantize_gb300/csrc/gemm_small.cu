@@ -46,9 +46,18 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kSlots = 3;
 constexpr int kRows = kSmallTileRows;  // routed rows per small tile (MMA N: up to 4 n8 fragments)
 constexpr int kBoxRows = 16;           // rows per activation box (one or two boxes per tile)
-constexpr int kChunkBlocks = 4;    // weight blocks per chunk of the tiled pack
+// weight blocks per chunk of the tiled pack: chunk_blocks(format) -- 4, or 2
+// for Q8_0; a 256-row chunk stays within 18 KB
 constexpr int kChunkVals = 256;    // K values per activation box (a W2 chunk; a W4NL chunk uses 128)
-constexpr int kRawBytes = kChunkBlocks * kTN * kBlockBytes;  // 18,432
+constexpr int kRawBytes = 4 * kTN * kBlockBytes;              // 18,432
+static_assert(chunk_blocks(MOE_FMT_Q8_0) * kTN * kQ8Bytes <= kRawBytes, "Q8_0 chunk fits a slot");
+// scales per row of an activation-scale box: a chunk's q8 blocks, at least 4
+// (a TMA box row is a multiple of 16 bytes and starts 16-byte aligned: a
+// 2-block Q8_0 chunk takes the aligned box of 4 holding its two scales)
+__host__ __device__ constexpr int dx_width(int fmt) {
+  return chunk_blocks(fmt) * block_values(fmt) / 32 > 4 ? chunk_blocks(fmt) * block_values(fmt) / 32
+                                                        : 4;
+}
 constexpr int kActBytes = kRows * kChunkVals * 2;       // 16,384: 32 rows x 256 fp16
 constexpr int kDxBytes = kRows * (kChunkVals / 32) * 4;  // 1,024: 32 rows x 8 scales
 // slots 1024-byte aligned: the activation boxes use the 128-byte swizzle
@@ -77,7 +86,7 @@ struct SmArgs {
   const int4* tiles;
   const int32_t* ntiles;  // {tiles, big-expert tiles}
   int E;
-  int K, N_out, bpr;
+  int K, N_out, bpr, bb;  // bb: bytes per weight block
   float* out;
   int gu_layout;
   __half* hq;
@@ -135,6 +144,13 @@ __device__ __forceinline__ uint32_t w2_pair_hi(uint32_t ws) {
   return hsub2_u32((ws & 0x03000300u) | 0x64006400u, 0x66006600u);  // (1024 + 256c) - 1536
 }
 constexpr uint32_t kHalfInv256 = 0x1C001C00u;  // fp16 pair (1/256, 1/256)
+// Q8_0: the fp16 pair (q_n, q_{n+8}) of two code words: byte sel selects code
+// n of lo and code n+8 of hi into bytes 0 and 2; each byte, sign bit flipped,
+// becomes the low mantissa byte of 1024 + 128 + q, and 1152 comes off: exact.
+__device__ __forceinline__ uint32_t q8_pair(uint32_t lo, uint32_t hi, uint32_t sel) {
+  const uint32_t t = __byte_perm(lo, hi, sel);
+  return hsub2_u32((t & 0x00FF00FFu) ^ 0x64806480u, 0x64806480u);
+}
 // W4NL: the fp16 pair (T[idx_i], T[idx_{i+8}]) from the group's two words.
 __device__ __forceinline__ uint32_t w4_pair(uint32_t wlo, uint32_t whi, int i,
                                             const uint16_t* lut) {
@@ -154,7 +170,10 @@ __device__ __forceinline__ bool consume_item(const uint8_t* smem, uint64_t* full
                                              float (&acc)[2][4][4], Refill&& refill) {
   constexpr bool kW2 = (FMT == MOE_FMT_W2);
   constexpr int kBv = kW2 ? 64 : 32;        // values per weight block
-  constexpr int kVals = kChunkBlocks * kBv;  // K values per chunk
+  constexpr int kCB = chunk_blocks(FMT);     // weight blocks per chunk
+  constexpr int kCode = code_bytes(FMT);     // code bytes per (row, block)
+  constexpr int kVals = kCB * kBv;           // K values per chunk
+  constexpr int kDxW = dx_width(FMT);        // scales per dx row in the slot
   constexpr int kQpb = kBv / 32;             // q8 blocks per weight block
   const int g = lane >> 2, cq = lane & 3;
   const float zero[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -162,8 +181,9 @@ __device__ __forceinline__ bool consume_item(const uint8_t* smem, uint64_t* full
     const uint32_t slot = cc % kSlots;
     if (!mbar_wait(&full[slot], (cc / kSlots) & 1, s_abort, kTimeoutNs, false)) return false;
     const uint8_t* sp = smem + slot * kSlotBytes;
-    const int nbc = min(kChunkBlocks, bpr - c * kChunkBlocks);
-    const uint16_t* scl = reinterpret_cast<const uint16_t*>(sp + nbc * nw * 16);
+    const int nbc = min(kCB, bpr - c * kCB);
+    const uint16_t* scl = reinterpret_cast<const uint16_t*>(sp + nbc * nw * kCode);
+    const int dxo = (c * (kVals / 32)) & 3;  // this chunk's first scale in the dx box
     const uint8_t* act = sp + kRawBytes;  // [box][32 rows][128 B], 128-byte swizzle
     const float* dxs = reinterpret_cast<const float*>(sp + kRawBytes + kActBytes);
 #pragma unroll 1
@@ -193,8 +213,8 @@ __device__ __forceinline__ bool consume_item(const uint8_t* smem, uint64_t* full
             b[0][nt][1] = hmul2_u32(b[0][nt][1], kHalfInv256);
             b[1][nt][1] = hmul2_u32(b[1][nt][1], kHalfInv256);
           }
-          dx[nt][0] = dxs[(8 * nt + 2 * cq) * (kVals / 32) + qb];
-          dx[nt][1] = dxs[(8 * nt + 2 * cq + 1) * (kVals / 32) + qb];
+          dx[nt][0] = dxs[(8 * nt + 2 * cq) * kDxW + dxo + qb];
+          dx[nt][1] = dxs[(8 * nt + 2 * cq + 1) * kDxW + dxo + qb];
         }
 #pragma unroll
         for (int mt = 0; mt < 2; mt++) {
@@ -202,7 +222,7 @@ __device__ __forceinline__ bool consume_item(const uint8_t* smem, uint64_t* full
           uint32_t af[2][4];
 #pragma unroll
           for (int h = 0; h < 2; h++) {
-            const uint8_t* wrow = sp + (j * nw + rbase[mt] + g + 8 * h) * 16;
+            const uint8_t* wrow = sp + (j * nw + rbase[mt] + g + 8 * h) * kCode;
             if (kW2) {
               // code words of groups 2qq, 2qq+1 of the block
               const uint2 w = *reinterpret_cast<const uint2*>(wrow + 8 * qq);
@@ -211,6 +231,16 @@ __device__ __forceinline__ bool consume_item(const uint8_t* smem, uint64_t* full
               af[0][2 + h] = w2_pair_hi(ws0);
               af[1][h] = w2_pair_lo(ws1);
               af[1][2 + h] = w2_pair_hi(ws1);
+            } else if (FMT == MOE_FMT_Q8_0) {
+              // group ks = words 4ks..4ks+3: values cq, cq+8 in words 4ks, 4ks+2
+              // and cq+4, cq+12 in words 4ks+1, 4ks+3, byte cq of each
+              const uint4 w0 = reinterpret_cast<const uint4*>(wrow)[0];
+              const uint4 w1 = reinterpret_cast<const uint4*>(wrow)[1];
+              const uint32_t sel = (uint32_t)(cq | (cq << 4) | ((4 + cq) << 8) | ((4 + cq) << 12));
+              af[0][h] = q8_pair(w0.x, w0.z, sel);
+              af[0][2 + h] = q8_pair(w0.y, w0.w, sel);
+              af[1][h] = q8_pair(w1.x, w1.z, sel);
+              af[1][2 + h] = q8_pair(w1.y, w1.w, sel);
             } else {
               const uint4 w = *reinterpret_cast<const uint4*>(wrow);
               af[0][h] = w4_pair(w.x, w.y, cq, s_lut);
@@ -283,7 +313,7 @@ __device__ __forceinline__ void prod_seek(Producer& p, const SmArgs& a, int firs
     p.row0 = I.t.y;
     p.nw = I.nw;
     p.nbox = I.t.z > kBoxRows ? 2 : 1;
-    p.wbase = a.pack + I.off + (int64_t)I.wt * kTN * a.bpr * kBlockBytes;
+    p.wbase = a.pack + I.off + (int64_t)I.wt * kTN * a.bpr * a.bb;
     return;
   }
 }
@@ -292,21 +322,23 @@ __device__ __forceinline__ void prod_issue(Producer& p, uint8_t* smem, uint64_t*
                                            const SmArgs& a, const CUtensorMap* tmap,
                                            const CUtensorMap* tmap_d, int first, int total,
                                            int n_wtiles, int64_t mbytes, int nchunks) {
-  constexpr int kVals = kChunkBlocks * (FMT == MOE_FMT_W2 ? 64 : 32);
+  constexpr int kCB = chunk_blocks(FMT), kBB = block_bytes(FMT);
+  constexpr int kVals = kCB * block_values(FMT);
+  constexpr int kDxW = dx_width(FMT);
   const uint32_t slot = p.issued % kSlots;
   uint8_t* sp = smem + slot * kSlotBytes;
-  const int nbc = min(kChunkBlocks, a.bpr - p.c * kChunkBlocks);
-  const uint32_t raw = (uint32_t)(nbc * p.nw * kBlockBytes);
+  const int nbc = min(kCB, a.bpr - p.c * kCB);
+  const uint32_t raw = (uint32_t)(nbc * p.nw * kBB);
   mbar_arrive_expect_tx(&full[slot], raw + (uint32_t)(p.nbox * kBoxRows * kVals * 2) +
-                                         (uint32_t)(p.nbox * kBoxRows * (kVals / 32) * 4));
-  bulk_g2s(sp, p.wbase + (int64_t)p.c * kChunkBlocks * p.nw * kBlockBytes, raw, &full[slot]);
+                                         (uint32_t)(p.nbox * kBoxRows * kDxW * 4));
+  bulk_g2s(sp, p.wbase + (int64_t)p.c * kCB * p.nw * kBB, raw, &full[slot]);
   for (int hb = 0; hb < p.nbox; hb++) {
 #pragma unroll
     for (int bx = 0; bx < kVals / kActBox; bx++)
       tma_load_2d(sp + kRawBytes + bx * (kRows * kActBox * 2) + hb * (kBoxRows * 128), tmap,
                   p.c * kVals + bx * kActBox, p.row0 + kBoxRows * hb, &full[slot]);
-    tma_load_2d(sp + kRawBytes + kActBytes + hb * (kBoxRows * (kVals / 32) * 4), tmap_d,
-                p.c * (kVals / 32), p.row0 + kBoxRows * hb, &full[slot]);
+    tma_load_2d(sp + kRawBytes + kActBytes + hb * (kBoxRows * kDxW * 4), tmap_d,
+                (p.c * (kVals / 32)) & ~3, p.row0 + kBoxRows * hb, &full[slot]);
   }
   p.issued++;
   if (++p.c == nchunks) {
@@ -343,15 +375,15 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
     *s_abort = 0;
     fence_mbar_init();
   }
-  if (!kW2 && tid < 16) s_lut[tid] = c_nl4_half[tid];
+  if (FMT == MOE_FMT_W4NL && tid < 16) s_lut[tid] = c_nl4_half[tid];
   __syncthreads();
 
   const int n_wtiles = (a.N_out + kTN - 1) / kTN;
   const int nt_all = max(0, min(a.ntiles[0], (int)max_tiles(a.rows_max, a.E)));
   const int first = max(0, min(a.ntiles[1], nt_all));
   const int total = (nt_all - first) * n_wtiles;
-  const int nchunks = (a.bpr + kChunkBlocks - 1) / kChunkBlocks;
-  const int64_t mbytes = (int64_t)a.N_out * a.bpr * kBlockBytes;
+  const int nchunks = (a.bpr + chunk_blocks(FMT) - 1) / chunk_blocks(FMT);
+  const int64_t mbytes = (int64_t)a.N_out * a.bpr * a.bb;
 
   // ring: prefill every slot, then lane 0 of warp 0 refills a slot as soon
   // as all warps have released it
@@ -577,6 +609,7 @@ cudaError_t launch_gemm_small(const GemmArgs& g, cudaStream_t st) {
   a.K = g.K;
   a.N_out = g.N_out;
   a.bpr = g.K / block_values(g.fmt);
+  a.bb = block_bytes(g.fmt);
   a.out = g.out;
   a.gu_layout = g.gu_layout;
   a.hq = g.hq;
@@ -588,7 +621,7 @@ cudaError_t launch_gemm_small(const GemmArgs& g, cudaStream_t st) {
   if (!encode) return cudaErrorNotSupported;
   // activations: [rows_max x K] fp16, boxes of 64 values (128 B, 128-byte
   // swizzle) x 16 rows, one chunk's worth per chunk
-  const int vals = kChunkBlocks * block_values(g.fmt);
+  const int vals = chunk_blocks(g.fmt) * block_values(g.fmt);
   CUtensorMap tm, td;
   const cuuint64_t dims[2] = {(cuuint64_t)g.K, (cuuint64_t)g.rows_max};
   const cuuint64_t strides[1] = {(cuuint64_t)g.K * 2};
@@ -598,11 +631,12 @@ cudaError_t launch_gemm_small(const GemmArgs& g, cudaStream_t st) {
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  // their scales: [rows_max x scale_stride(K)] fp32, boxes of 8 (W2) or 4 blocks x 16 rows
+  // their scales: [rows_max x scale_stride(K)] fp32, boxes of dx_width (8 for
+  // W2, 4 otherwise) x 16 rows
   const int ss = scale_stride(g.K);
   const cuuint64_t ddims[2] = {(cuuint64_t)ss, (cuuint64_t)g.rows_max};
   const cuuint64_t dstrides[1] = {(cuuint64_t)ss * 4};
-  const cuuint32_t dbox[2] = {(cuuint32_t)(vals / 32), (cuuint32_t)kBoxRows};
+  const cuuint32_t dbox[2] = {(cuuint32_t)dx_width(g.fmt), (cuuint32_t)kBoxRows};
   if (encode(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(g.act_d), ddims, dstrides,
              dbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -618,10 +652,14 @@ cudaError_t launch_gemm_small(const GemmArgs& g, cudaStream_t st) {
     e = mode == kModeDown     ? launch_small<MOE_FMT_W2, kModeDown>(a, tm, td, items_max, st)
         : mode == kModeSwiglu ? launch_small<MOE_FMT_W2, kModeSwiglu>(a, tm, td, items_max, st)
                               : launch_small<MOE_FMT_W2, kModeGU>(a, tm, td, items_max, st);
-  } else {
+  } else if (g.fmt == MOE_FMT_W4NL) {
     e = mode == kModeDown     ? launch_small<MOE_FMT_W4NL, kModeDown>(a, tm, td, items_max, st)
         : mode == kModeSwiglu ? launch_small<MOE_FMT_W4NL, kModeSwiglu>(a, tm, td, items_max, st)
                               : launch_small<MOE_FMT_W4NL, kModeGU>(a, tm, td, items_max, st);
+  } else {
+    e = mode == kModeDown     ? launch_small<MOE_FMT_Q8_0, kModeDown>(a, tm, td, items_max, st)
+        : mode == kModeSwiglu ? launch_small<MOE_FMT_Q8_0, kModeSwiglu>(a, tm, td, items_max, st)
+                              : launch_small<MOE_FMT_Q8_0, kModeGU>(a, tm, td, items_max, st);
   }
   if (e != cudaSuccess) return e;
   count_launch();

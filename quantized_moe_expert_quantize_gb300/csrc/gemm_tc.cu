@@ -75,8 +75,8 @@ constexpr int kTN = 256;          // weight rows per tile (MMA N, TMEM columns)
 constexpr int kSK = 64;           // K values per stage (one 128-byte swizzle row of fp16)
 constexpr int kStages = 3;
 constexpr int kTBufs = 2;         // TMEM accumulator buffers of kTN columns
-constexpr int kChunkBlocks = 4;   // weight blocks per raw chunk of the tiled pack
-constexpr int kRawSlot = kChunkBlocks * kTN * kBlockBytes;  // 18 KB
+constexpr int kRawSlot = 4 * kTN * kBlockBytes;  // one raw chunk of the tiled pack: 18 KB
+static_assert(chunk_blocks(MOE_FMT_Q8_0) * kTN * kQ8Bytes <= kRawSlot, "Q8_0 chunk fits a slot");
 constexpr int kDxRing = 8;        // activation-scale entries of 4 blocks x 128 rows
 constexpr int kDwRing = 16;       // W4NL weight scales, one entry per 32-value block
 constexpr int kScaleBox = 4;      // scale columns per TMA box: 16 bytes a row
@@ -141,6 +141,7 @@ struct TcArgs {
   int K;
   int N_out;
   int bpr;              // weight blocks per row
+  int bb;               // bytes per weight block
   float* out;           // GU [rows x N_out] (gate/up columns in layout gu_layout) or Dm
   int gu_layout;        // MOE_GU_*
   __half* hq;           // fused swiglu_quant: Hq [rows x N_out/2], pair-interleaved
@@ -170,9 +171,9 @@ __device__ __forceinline__ Item make_item(const TcArgs& a, const int64_t* s_eoff
   const bool rows_ok = (unsigned)it.e < (unsigned)a.E && it.row0 >= 0 && it.nrows > 0 &&
                        it.nrows <= kTM && (int64_t)it.row0 + it.nrows <= a.rows_max;
   const int64_t off = rows_ok ? s_eoff[it.e] : -1;
-  const int64_t mbytes = (int64_t)a.N_out * a.bpr * kBlockBytes;
+  const int64_t mbytes = (int64_t)a.N_out * a.bpr * a.bb;
   it.ok = rows_ok && off >= 0 && (off & 15) == 0 && off + mbytes <= a.pack_bytes;
-  it.wbase = it.ok ? a.pack + off + (int64_t)it.o0 * a.bpr * kBlockBytes : nullptr;
+  it.wbase = it.ok ? a.pack + off + (int64_t)it.o0 * a.bpr * a.bb : nullptr;
   return it;
 }
 
@@ -247,6 +248,37 @@ __device__ __forceinline__ void decode_w4_store(uint4 codes, const uint16_t* lut
   }
 }
 
+// fp16 pair (q_n, q_{n+8}) of two Q8_0 code words: byte sel selects code n
+// of lo and code n+8 of hi into bytes 0 and 2; each byte, sign bit flipped,
+// becomes the low mantissa byte of 1024 + 128 + q, and 1152 comes off: exact.
+__device__ __forceinline__ uint32_t q8_pair(uint32_t lo, uint32_t hi, uint32_t sel) {
+  const uint32_t t = __byte_perm(lo, hi, sel);
+  return hsub2_u32((t & 0x00FF00FFu) ^ 0x64806480u, 0x64806480u);
+}
+
+// Decode one Q8_0 block (32 int8 codes; word w holds codes 4w..4w+3) into
+// 16-byte chunks 4*kb .. 4*kb+3 of operand row r: fp16 integers,
+// pair-interleaved like the other formats.
+__device__ __forceinline__ void decode_q8_store(const uint4* codes, uint8_t* tile, int r, int kb) {
+  const uint4 a = codes[0], b = codes[1];
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int g = 0; g < 2; g++) {
+#pragma unroll
+    for (int half = 0; half < 2; half++) {
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        // values n = 4*half + i and n + 8 of group g: byte i of words
+        // 4g + half and 4g + 2 + half
+        const uint32_t sel = (uint32_t)(i | (i << 4) | ((4 + i) << 8) | ((4 + i) << 12));
+        o[i] = q8_pair(w[4 * g + half], w[4 * g + 2 + half], sel);
+      }
+      st_swizzled(tile, r, 4 * kb + 2 * g + half, o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
 // ------------------------------------------------------------- epilogue
 // 32-byte store of 8 consecutive fp32 values (4 packed pairs); p 32-byte aligned.
 __device__ __forceinline__ void st_global_v8(float* p, const float2* v) {
@@ -305,7 +337,10 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
   constexpr bool kFold = (FMT == MOE_FMT_W2);
   constexpr bool kDown = (MODE == kModeDown);
   constexpr int kBps = kFold ? 1 : 2;                  // weight blocks per stage
-  constexpr int kSpc = kChunkBlocks / kBps;            // stages per raw chunk
+  constexpr int kCB = chunk_blocks(FMT);               // weight blocks per raw chunk
+  constexpr int kCode = code_bytes(FMT);               // code bytes per (row, block)
+  constexpr int kBB = block_bytes(FMT);
+  constexpr int kSpc = kCB / kBps;                     // stages per raw chunk
 
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, offset from the shared array itself (an integer
@@ -368,7 +403,7 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
     tc_fence_before();
   }
   for (int e = tid; e < a.E; e += kThreads) s_eoff[e] = a.eoff[2 * e + a.which];
-  if (!kFold && tid < 16) s_lut[tid] = c_nl4_half[tid];
+  if (FMT == MOE_FMT_W4NL && tid < 16) s_lut[tid] = c_nl4_half[tid];
   __syncthreads();
   tc_fence_after();
 
@@ -528,13 +563,13 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
           slot = cc & 1;
           if (!(alive = mbar_wait(&rfull[slot], (cc >> 1) & 1, s_abort, kTimeoutNs))) break;
           raw = sRaw + slot * kRawSlot;
-          nbc = min(kChunkBlocks, a.bpr - (s / kSpc) * kChunkBlocks);
+          nbc = min(kCB, a.bpr - (s / kSpc) * kCB);
         }
         const int st = it % kStages;
         if (!(alive = mbar_wait(&empty[st], ((it / kStages) & 1) ^ 1, s_abort, kTimeoutNs))) break;
         uint8_t* tileB = sB + st * kBBytes;
         const uint8_t* codes = raw;
-        const uint16_t* scales = reinterpret_cast<const uint16_t*>(raw + nbc * I.NW * 16);
+        const uint16_t* scales = reinterpret_cast<const uint16_t*>(raw + nbc * I.NW * kCode);
         if (kFold) {
 #pragma unroll
           for (int rr = 0; rr < 2; rr++) {
@@ -558,8 +593,12 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
               const int r = t + 128 * rr;
               if (r < I.NW) {
                 const int idx = (2 * sc + kb) * I.NW + r;
-                decode_w4_store(*reinterpret_cast<const uint4*>(codes + idx * 16), s_lut, tileB,
-                                r, kb);
+                if (FMT == MOE_FMT_W4NL)
+                  decode_w4_store(*reinterpret_cast<const uint4*>(codes + idx * kCode), s_lut,
+                                  tileB, r, kb);
+                else
+                  decode_q8_store(reinterpret_cast<const uint4*>(codes + idx * kCode), tileB, r,
+                                  kb);
                 sDw[(w % kDwRing) * kTN + r] = __half2float(__ushort_as_half(scales[idx]));
               }
             }
@@ -629,7 +668,7 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
     // one bulk copy per (256-row tile, 4-block chunk), into two slots
     setmaxnreg_dec<Regs<FMT>::other>();
     if (lane == 0) {
-      const int chunks_per_item = (a.bpr + kChunkBlocks - 1) / kChunkBlocks;
+      const int chunks_per_item = (a.bpr + kCB - 1) / kCB;
       uint32_t issued = 0;
       bool alive = true;
       for (int64_t item = blockIdx.x; item < total && alive; item += stride) {
@@ -640,10 +679,10 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
           const uint32_t slot = issued & 1;
           if (!(alive = mbar_wait(&rempty[slot], ((issued >> 1) & 1) ^ 1, s_abort, kTimeoutNs)))
             break;
-          const int nbc = min(kChunkBlocks, a.bpr - c * kChunkBlocks);
-          const uint32_t bytes = (uint32_t)(nbc * I.NW * kBlockBytes);
+          const int nbc = min(kCB, a.bpr - c * kCB);
+          const uint32_t bytes = (uint32_t)(nbc * I.NW * kBB);
           mbar_arrive_expect_tx(&rfull[slot], bytes);
-          bulk_g2s(sRaw + slot * kRawSlot, I.wbase + (int64_t)c * kChunkBlocks * I.NW * kBlockBytes,
+          bulk_g2s(sRaw + slot * kRawSlot, I.wbase + (int64_t)c * kCB * I.NW * kBB,
                    bytes, &rfull[slot]);
         }
       }
@@ -763,6 +802,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
   a.E = g.E;
   a.K = g.K;
   a.N_out = g.N_out;
+  a.bb = block_bytes(g.fmt);
   a.bpr = g.K / block_values(g.fmt);
   a.out = g.out;
   a.hq = g.hq;
@@ -804,10 +844,14 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
     if (mode == kModeDown) { MOE_LAUNCH_TC(MOE_FMT_W2, kModeDown) }
     else if (mode == kModeSwiglu) { MOE_LAUNCH_TC(MOE_FMT_W2, kModeSwiglu) }
     else { MOE_LAUNCH_TC(MOE_FMT_W2, kModeGU) }
-  } else {
+  } else if (g.fmt == MOE_FMT_W4NL) {
     if (mode == kModeDown) { MOE_LAUNCH_TC(MOE_FMT_W4NL, kModeDown) }
     else if (mode == kModeSwiglu) { MOE_LAUNCH_TC(MOE_FMT_W4NL, kModeSwiglu) }
     else { MOE_LAUNCH_TC(MOE_FMT_W4NL, kModeGU) }
+  } else {
+    if (mode == kModeDown) { MOE_LAUNCH_TC(MOE_FMT_Q8_0, kModeDown) }
+    else if (mode == kModeSwiglu) { MOE_LAUNCH_TC(MOE_FMT_Q8_0, kModeSwiglu) }
+    else { MOE_LAUNCH_TC(MOE_FMT_Q8_0, kModeGU) }
   }
 #undef MOE_LAUNCH_TC
   count_launch();

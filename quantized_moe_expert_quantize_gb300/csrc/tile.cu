@@ -9,10 +9,11 @@
 //     n_ff+128t .. n_ff+128t+NW/2-1 (a tile yields whole blocks of H) --
 //     gate row g is row g of the source matrix and up row g is row n_ff+g
 //     (split layout), or rows 2g and 2g+1 (interleaved layout);
-//   chunk c of a tile covers blocks 4c .. 4c+nbc-1, nbc = min(4, bpr - 4c),
-//     at byte 4 * c * NW * 18 of the tile;
-//   inside a chunk: the 16 code bytes of (row r, block j) at (j*NW + r)*16,
-//     then the fp16 scales at nbc*NW*16 + (j*NW + r)*2.
+//   chunk c of a tile covers blocks cb*c .. cb*c+nbc-1 (cb = 4 blocks, 2 for
+//     Q8_0), nbc = min(cb, bpr - cb*c), at byte cb * c * NW * BB of the tile
+//     (BB = 18 bytes a block, 34 for Q8_0; the tile at 256 * t * bpr * BB);
+//   inside a chunk: the CB code bytes (16, or 32 for Q8_0) of (row r, block
+//     j) at (j*NW + r)*CB, then the fp16 scales at nbc*NW*CB + (j*NW + r)*2.
 // Expert e's gate/up matrix starts at e*(gu_bytes + down_bytes), its down
 // matrix gu_bytes later.  Every chunk starts 16-byte aligned.
 #include <algorithm>
@@ -31,6 +32,7 @@ struct TileJob {
   int32_t* status;          // may be null
   int E;
   int gu_layout;            // MOE_GU_*
+  int fmt[2];
   int N[2], K[2], bpr[2];
   int64_t mbytes[2];        // bytes of one matrix
 };
@@ -65,27 +67,25 @@ __global__ void tile_weights_kernel(const TileJob j) {
       t = gr >> 7;
       r = (gr & 127) + (up ? min(128, n_ff - 128 * t) : 0);
     }
+    const int fmt = j.fmt[which];
+    const int bb = block_bytes(fmt), cbytes = code_bytes(fmt), cb = chunk_blocks(fmt);
     const int nw = min(256, j.N[which] - 256 * t);
-    const int c = blk >> 2, jj = blk & 3, nbc = min(4, bpr - 4 * c);
-    const int64_t chunk = dbase + (int64_t)256 * t * bpr * kBlockBytes +
-                          (int64_t)4 * c * nw * kBlockBytes;
-    uint8_t* codes = j.dst + chunk + ((int64_t)jj * nw + r) * 16;
-    uint16_t* scale = reinterpret_cast<uint16_t*>(j.dst + chunk + (int64_t)nbc * nw * 16 +
+    const int c = blk / cb, jj = blk - c * cb, nbc = min(cb, bpr - cb * c);
+    const int64_t chunk = dbase + (int64_t)256 * t * bpr * bb + (int64_t)cb * c * nw * bb;
+    uint8_t* codes = j.dst + chunk + ((int64_t)jj * nw + r) * cbytes;
+    uint16_t* scale = reinterpret_cast<uint16_t*>(j.dst + chunk + (int64_t)nbc * nw * cbytes +
                                                   ((int64_t)jj * nw + r) * 2);
-    uint16_t h[9];
-    if (ok) {
-      const uint16_t* s = reinterpret_cast<const uint16_t*>(
-          j.src + soff + ((int64_t)row * bpr + blk) * kBlockBytes);
+    // the block's 2-byte words: scale, then the codes (8 or 16 words)
+    const uint16_t* s = reinterpret_cast<const uint16_t*>(
+        j.src + soff + ((int64_t)row * bpr + blk) * bb);
+    *scale = ok ? s[0] : 0;
+    for (int q = 0; q < cbytes / 16; q++) {
+      uint32_t w[4];
 #pragma unroll
-      for (int k = 0; k < 9; k++) h[k] = s[k];
-    } else {
-#pragma unroll
-      for (int k = 0; k < 9; k++) h[k] = 0;
+      for (int k = 0; k < 4; k++)
+        w[k] = ok ? ((uint32_t)s[1 + 8 * q + 2 * k] | ((uint32_t)s[2 + 8 * q + 2 * k] << 16)) : 0u;
+      reinterpret_cast<uint4*>(codes)[q] = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    *scale = h[0];
-    *reinterpret_cast<uint4*>(codes) =
-        make_uint4((uint32_t)h[1] | ((uint32_t)h[2] << 16), (uint32_t)h[3] | ((uint32_t)h[4] << 16),
-                   (uint32_t)h[5] | ((uint32_t)h[6] << 16), (uint32_t)h[7] | ((uint32_t)h[8] << 16));
   }
 }
 
@@ -110,6 +110,8 @@ cudaError_t launch_tile_weights(const MoeLayerDesc& d, const uint8_t* src, int64
   j.status = status;
   j.E = d.E;
   j.gu_layout = d.gu_layout;
+  j.fmt[0] = d.gu_fmt;
+  j.fmt[1] = d.down_fmt;
   j.N[0] = 2 * d.n_ff;
   j.K[0] = d.d;
   j.N[1] = d.d;

@@ -53,7 +53,7 @@ def test_workspace_bytes_layout(lib):
 @pytest.mark.parametrize("field,value,code", [
     ("d", 100, M.MOE_ERR_SHAPE), ("d", 32, M.MOE_ERR_SHAPE), ("n_ff", 96, M.MOE_ERR_SHAPE),
     ("E", 0, M.MOE_ERR_SHAPE), ("E", 2048, M.MOE_ERR_SHAPE), ("k", 0, M.MOE_ERR_SHAPE),
-    ("k", 9, M.MOE_ERR_SHAPE), ("T", -1, M.MOE_ERR_SHAPE), ("gu_fmt", 3, M.MOE_ERR_FORMAT),
+    ("k", 9, M.MOE_ERR_SHAPE), ("T", -1, M.MOE_ERR_SHAPE), ("gu_fmt", 4, M.MOE_ERR_FORMAT),
     ("down_fmt", 0, M.MOE_ERR_FORMAT), ("gu_layout", 2, M.MOE_ERR_FORMAT),
     ("flags", 1, M.MOE_ERR_FORMAT)])
 def test_bad_descriptor_rejected(lib, field, value, code):

@@ -40,6 +40,16 @@ SMALL = {
     "mid_w4nl_w2_inter": lambda: synth.make_layer(
         synth.LayerShape(257, 384, 128, 12, 3, synth.W4NL, synth.W2, synth.GU_INTERLEAVED),
         seed=8, routing="topk", bias=True, outliers=True),
+    # Q8_0 down (and gate/up) matrices
+    "mid_w2_q8": lambda: synth.make_layer(
+        synth.LayerShape(300, 512, 192, 16, 4, synth.W2, synth.Q8_0),
+        seed=14, routing="topk", bias=True, outliers=True),
+    "mid_q8_q8_inter": lambda: synth.make_layer(
+        synth.LayerShape(257, 384, 128, 12, 3, synth.Q8_0, synth.Q8_0, synth.GU_INTERLEAVED),
+        seed=15, routing="topk", bias=True, outliers=True),
+    "flat_w4nl_q8": lambda: synth.make_layer(
+        synth.LayerShape(128, 256, 128, 16, 4, synth.W4NL, synth.Q8_0),
+        seed=16, routing="flat", outliers=True),
 }
 
 
@@ -100,7 +110,7 @@ def test_interleaved_gate_up_equals_split(M):
 
 
 @pytest.mark.parametrize("name", ["mid_w2_w2", "mid_w2_w4nl", "mid_w4nl_w4nl", "flat_w2_w4nl",
-                                  "mid_w2_w2_inter"])
+                                  "mid_w2_w2_inter", "mid_q8_q8_inter"])
 def test_fused_swiglu_equals_stages(M, name):
     """The layer's gate/up epilogue with swiglu_quant fused writes the same Hq
     and dh bits as the gate/up stage followed by the swiglu_quant stage."""
@@ -326,7 +336,9 @@ def _tile_reference(pack, eoff, fmt_gu, fmt_dn, d, n_ff, E, gu_layout=synth.GU_S
     for e in range(E):
         for which, (fmt, N, K) in enumerate(((fmt_gu, 2 * n_ff, d), (fmt_dn, d, n_ff))):
             bpr = K // synth.BLOCK_VALUES[fmt]
-            m = pack[eoff[e, which]:eoff[e, which] + N * bpr * 18].reshape(N, bpr, 18)
+            bb = synth.BLOCK_BYTES_OF[fmt]
+            cb = 2 if fmt == synth.Q8_0 else 4         # blocks per chunk
+            m = pack[eoff[e, which]:eoff[e, which] + N * bpr * bb].reshape(N, bpr, bb)
             if which == 0 and gu_layout == synth.GU_INTERLEAVED:
                 gate, up = m[0::2], m[1::2]
             else:
@@ -338,8 +350,8 @@ def _tile_reference(pack, eoff, fmt_gu, fmt_dn, d, n_ff, E, gu_layout=synth.GU_S
                     rows = np.concatenate([gate[g0:g0 + nw // 2], up[g0:g0 + nw // 2]])
                 else:
                     rows = m[t:t + nw]
-                for c in range(0, bpr, 4):
-                    blk = rows[:, c:c + 4]                     # [nw, nbc, 18]
+                for c in range(0, bpr, cb):
+                    blk = rows[:, c:c + cb]                    # [nw, nbc, bb]
                     out.append(blk[:, :, 2:].transpose(1, 0, 2).reshape(-1))
                     out.append(blk[:, :, :2].transpose(1, 0, 2).reshape(-1))
     return np.concatenate(out)
@@ -348,7 +360,8 @@ def _tile_reference(pack, eoff, fmt_gu, fmt_dn, d, n_ff, E, gu_layout=synth.GU_S
 @pytest.mark.parametrize("shape", [synth.LayerShape(8, 384, 192, 3, 2, synth.W2, synth.W4NL),
                                    synth.LayerShape(8, 640, 320, 2, 1, synth.W4NL, synth.W2),
                                    synth.LayerShape(8, 384, 192, 3, 2, synth.W2, synth.W2,
-                                                    synth.GU_INTERLEAVED)])
+                                                    synth.GU_INTERLEAVED),
+                                   synth.LayerShape(8, 640, 320, 2, 1, synth.Q8_0, synth.Q8_0)])
 def test_tiled_pack_layout(M, shape):
     """moe_tile_weights writes exactly the documented byte permutation, with
     ragged last tiles (N_out % 256 == 128) and ragged last chunks."""
