@@ -141,7 +141,6 @@ struct TcArgs {
   int K;
   int N_out;
   int bpr;              // weight blocks per row
-  int bb;               // bytes per weight block
   float* out;           // GU [rows x N_out] (gate/up columns in layout gu_layout) or Dm
   int gu_layout;        // MOE_GU_*
   __half* hq;           // fused swiglu_quant: Hq [rows x N_out/2], pair-interleaved
@@ -160,8 +159,10 @@ struct Item {
 // against weight-row tile item % n_wtiles.  Everything read from the work
 // list is bounds-checked: a list not written by the routing step (stage API
 // misuse) is skipped, never followed.
+template <int FMT>
 __device__ __forceinline__ Item make_item(const TcArgs& a, const int64_t* s_eoff, int4 t,
                                           int wtile) {
+  constexpr int kBB = block_bytes(FMT);
   Item it;
   it.e = t.x;
   it.row0 = t.y;
@@ -171,9 +172,9 @@ __device__ __forceinline__ Item make_item(const TcArgs& a, const int64_t* s_eoff
   const bool rows_ok = (unsigned)it.e < (unsigned)a.E && it.row0 >= 0 && it.nrows > 0 &&
                        it.nrows <= kTM && (int64_t)it.row0 + it.nrows <= a.rows_max;
   const int64_t off = rows_ok ? s_eoff[it.e] : -1;
-  const int64_t mbytes = (int64_t)a.N_out * a.bpr * a.bb;
+  const int64_t mbytes = (int64_t)a.N_out * a.bpr * kBB;
   it.ok = rows_ok && off >= 0 && (off & 15) == 0 && off + mbytes <= a.pack_bytes;
-  it.wbase = it.ok ? a.pack + off + (int64_t)it.o0 * a.bpr * a.bb : nullptr;
+  it.wbase = it.ok ? a.pack + off + (int64_t)it.o0 * a.bpr * kBB : nullptr;
   return it;
 }
 
@@ -431,7 +432,7 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
     bool alive = true;
     for (int item = blockIdx.x; item < (int)total && alive; item += (int)stride) {
       const int wtile = item % n_wtiles;
-      const Item I = make_item(a, s_eoff, load_tile(a, item, total, n_wtiles), wtile);
+      const Item I = make_item<FMT>(a, s_eoff, load_tile(a, item, total, n_wtiles), wtile);
       if (!I.ok) {
         if (lane == 0 && warp == 0) atomicOr(a.status, MOE_STATUS_BAD_OFFSET);
         continue;
@@ -551,7 +552,7 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
     bool alive = true;
     for (int64_t item = blockIdx.x; item < total && alive; item += stride) {
       // (this role runs ahead of the MMA; its per-item load latency is hidden)
-      const Item I = make_item(a, s_eoff, load_tile(a, item, total, n_wtiles),
+      const Item I = make_item<FMT>(a, s_eoff, load_tile(a, item, total, n_wtiles),
                                (int)(item % n_wtiles));
       if (!I.ok) continue;
       const uint8_t* raw = nullptr;
@@ -625,7 +626,7 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
       uint32_t it = 0;
       bool alive = true;
       for (int64_t item = blockIdx.x; item < total && alive; item += stride) {
-        const Item I = make_item(a, s_eoff, load_tile(a, item, total, n_wtiles),
+        const Item I = make_item<FMT>(a, s_eoff, load_tile(a, item, total, n_wtiles),
                                  (int)(item % n_wtiles));
         if (!I.ok) continue;
         for (int s = 0; s < nstages; s++, it++) {
@@ -649,7 +650,7 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
       uint32_t gd = 0;
       bool alive = true;
       for (int64_t item = blockIdx.x; item < total && alive; item += stride) {
-        const Item I = make_item(a, s_eoff, load_tile(a, item, total, n_wtiles),
+        const Item I = make_item<FMT>(a, s_eoff, load_tile(a, item, total, n_wtiles),
                                  (int)(item % n_wtiles));
         if (!I.ok) continue;
         for (int j = 0; j < (nb + 3) / 4; j++, gd++) {
@@ -672,7 +673,7 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
       uint32_t issued = 0;
       bool alive = true;
       for (int64_t item = blockIdx.x; item < total && alive; item += stride) {
-        const Item I = make_item(a, s_eoff, load_tile(a, item, total, n_wtiles),
+        const Item I = make_item<FMT>(a, s_eoff, load_tile(a, item, total, n_wtiles),
                                  (int)(item % n_wtiles));
         if (!I.ok) continue;
         for (int c = 0; c < chunks_per_item; c++, issued++) {
@@ -696,7 +697,7 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
       bool alive = true;
       int4 tnext = load_tile(a, blockIdx.x, total, n_wtiles);
       for (int64_t item = blockIdx.x; item < total && alive; item += stride) {
-        const Item I = make_item(a, s_eoff, tnext, (int)(item % n_wtiles));
+        const Item I = make_item<FMT>(a, s_eoff, tnext, (int)(item % n_wtiles));
         tnext = load_tile(a, item + stride, total, n_wtiles);
         if (!I.ok) continue;
         const uint32_t idesc = idesc_f16_f32(kTM, I.NW);  // M = routed rows, N = weight rows
@@ -802,7 +803,6 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
   a.E = g.E;
   a.K = g.K;
   a.N_out = g.N_out;
-  a.bb = block_bytes(g.fmt);
   a.bpr = g.K / block_values(g.fmt);
   a.out = g.out;
   a.hq = g.hq;
