@@ -46,7 +46,7 @@ INT8_MMA_PEAK_TOPS = 150.0
 # launch) at configuration 2 (ncu, one pass: profiles/dram_gate_up_T16384.md),
 # valid while the product kernels' sources hash as they did at capture
 TRAFFIC_GATE_UP = {2: 1.5877e9}
-TRAFFIC_SOURCES_SHA = "2e089115fead15d0"
+TRAFFIC_SOURCES_SHA = "2e7c5f46c4473d26"
 TRAFFIC_SOURCES = ("gemm_tc.cu", "gemm_small.cu", "route.cu", "sm100_ptx.cuh", "common.cuh")
 ALGO_BYTES_GATE_UP = {2: 1.586e9}
 
