@@ -411,3 +411,10 @@ def test_launch_counter_counts(M):
     n0 = M.moe_kernel_launches()
     dl.run_layer()
     assert M.moe_kernel_launches() - n0 >= 6
+
+
+def test_smoke_entry_point(M):
+    """__graft_entry__.smoke(): the tiny layer through the C ABI against the
+    oracle (tiled weights, routed-row q8, Hq and out tolerances)."""
+    import __graft_entry__
+    __graft_entry__.smoke()
