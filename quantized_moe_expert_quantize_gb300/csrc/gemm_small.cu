@@ -1,31 +1,35 @@
 // Small-row tier of the grouped expert products: tiles of at most
-// kSmallTileRows (32) routed rows.
+// kSmallTileRows (32) routed rows -- experts with few rows, and the short
+// remainder of every expert after its full 128-row tiles.
 //
 // Same arithmetic as the tcgen05 kernel -- per 32-value K block the exact
 // integer sum of w_int * q, then the fp32 epilogue in K order ("Strata #3752",
 // commit "moe_ws kernels") -- on a different tile shape.  With a handful of
-// rows per expert the layer streams weights: each expert's whole weight matrix
-// is read for a few rows, so the time is the weight bytes (the pages tune a
-// separate tier by rows per expert, "Strata #3752", addendum).  A 128-row
-// tcgen05 tile would compute mostly padding; here the weights are the MMA's
-// M side, decoded straight into mma.sync.m16n8k16 fp16 fragments in
-// registers, and the few routed rows are its N side (8 per fragment), with
-// fp32 accumulators in registers.  Operands are exact fp16 integers (|w|,
-// |q| <= 127; W2 with its scale folded, d*(c-2) exact), so each 16-value
-// MMA step and each 32-value block sum is exact in fp32.
+// rows per expert the work is a weight stream: each expert's weight tile is
+// read for a few rows (the pages tune a separate tier by rows per expert,
+// "Strata #3752", addendum).  A 128-row tcgen05 tile would compute mostly
+// padding at the cost of a full one; here the weights are the M side of
+// mma.sync.m16n8k16, decoded into fp16 fragments in registers, and the routed
+// rows are its N side (1 to 4 fragments of 8), with fp32 accumulators in
+// registers.  The A values are exact fp16 integers (W2: c-2, or 256*(c-2)
+// against B values pre-scaled by 1/256; W4NL: the table; Q8_0: the code) and
+// the B values the q8 integers, so every product and every 32-value block
+// sum is exact in fp32; the weight scale enters in the epilogue, where
+// d_w * isum is exact for W2.
 //
-// Item: one small expert's rows (one tile of the work list) against one
-// 256-row tile of the tiled weight pack.  4 compute warps own 64 tile rows
-// each (4 m16 fragments); warp 4 produces: per 4-block weight chunk one bulk
-// copy of the raw chunk and one 2-D TMA box each of the 16 activation rows
-// and their scales, into a ring of 4 slots.
+// Item: one small-row tile of the work list against one 256-row tile of the
+// tiled weight pack.  8 warps own 32 tile rows each (2 m16 fragments; for
+// gate/up, 16 gate rows and the matching up rows).  Two CTAs run on each
+// multiprocessor.  A 3-slot ring holds per slot one weight chunk (one bulk
+// copy) and the tile's activation rows and scales (2-D TMA boxes of 16 rows);
+// lane 0 of warp 0 refills a slot once all 8 warps have released it.
 //
 // The routed rows' activations are stored pair-interleaved in every 16-value
 // group (position 2i holds value i, 2i+1 holds value i+8).  Taking the MMA's
-// k as the stored position, a thread's A-fragment pairs are the weights of
-// values (c, c+8) and (c+4, c+12) of a group -- exactly the pairs one code
-// word yields with one mask per pair -- and its B-fragment pairs are single
-// 32-bit words of the stored rows.
+// k as the stored position, a lane's A-fragment pairs are the weights of
+// values (c, c+8) and (c+4, c+12) of a group -- pairs that one code word
+// yields with one mask each -- and its B fragments come from ldmatrix on the
+// 128-byte-swizzled activation boxes.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 

@@ -20,8 +20,9 @@
 // exactly and the epilogue is one fma per (output, block):
 //     acc = fma(d_x, d_w*isum, acc)
 // -- one rounding where the plain statement rounds d_w*d_x first; the two
-// differ by at most an ulp per block.  W4NL weights (T[idx]*d is not exact
-// in fp16) keep the integer operand and the two-step epilogue
+// differ by at most an ulp per block.  W4NL and Q8_0 weights (T[idx]*d and
+// q*d are not exact in fp16) keep the integer operand and the two-step
+// epilogue
 //     acc = fma(d_w*d_x, isum, acc).
 //
 // Tiles: up to 128 routed rows of one expert (MMA M, the TMEM lanes; each
@@ -78,7 +79,7 @@ constexpr int kTBufs = 2;         // TMEM accumulator buffers of kTN columns
 constexpr int kRawSlot = 4 * kTN * kBlockBytes;  // one raw chunk of the tiled pack: 18 KB
 static_assert(chunk_blocks(MOE_FMT_Q8_0) * kTN * kQ8Bytes <= kRawSlot, "Q8_0 chunk fits a slot");
 constexpr int kDxRing = 8;        // activation-scale entries of 4 blocks x 128 rows
-constexpr int kDwRing = 16;       // W4NL weight scales, one entry per 32-value block
+constexpr int kDwRing = 16;       // W4NL / Q8_0 weight scales, one entry per 32-value block
 constexpr int kScaleBox = 4;      // scale columns per TMA box: 16 bytes a row
 constexpr int kEpiWarps = 16;
 constexpr int kWarpDecode = 16;   // warps 16..19
@@ -362,7 +363,7 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
   uint64_t* rempty = rfull + 2;               // [2]       decode warps done with the slot
   uint64_t* dfull = rempty + 2;               // [kDxRing] scale bytes landed
   uint64_t* dempty = dfull + kDxRing;         // [kDxRing] epilogue warps
-  uint64_t* wfull = dempty + kDxRing;         // [kDwRing] decode warps (W4NL scales)
+  uint64_t* wfull = dempty + kDxRing;         // [kDwRing] decode warps (W4NL / Q8_0 scales)
   uint64_t* wempty = wfull + kDwRing;         // [kDwRing] epilogue warps
   uint64_t* fin = wempty + kDwRing;           // MMA drain at exit
   int64_t* s_eoff = reinterpret_cast<int64_t*>(smem + kOffEoff);
