@@ -46,19 +46,28 @@ INT8_MMA_PEAK_TOPS = 150.0
 # launch) at configuration 2 (ncu, one pass: profiles/dram_gate_up_T16384.md),
 # valid while the product kernels' sources hash as they did at capture
 TRAFFIC_GATE_UP = {2: 1.5877e9}
-TRAFFIC_SOURCES_SHA = "2e7c5f46c4473d26"
+TRAFFIC_SOURCES_SHA = "0c5a7146ca560c87"
 TRAFFIC_SOURCES = ("gemm_tc.cu", "gemm_small.cu", "route.cu", "sm100_ptx.cuh", "common.cuh")
 ALGO_BYTES_GATE_UP = {2: 1.586e9}
 
 
-def measured_traffic(config: int):
+def sources_sha() -> str:
+    """sha256 (first 16 hex digits) of the product kernels' code: the files of
+    TRAFFIC_SOURCES with // comments, trailing blanks and empty lines taken
+    out, so that only a change of code invalidates a capture."""
     import hashlib
+    import re
     csrc = os.path.join(ROOT, "quantized_moe_expert_quantize_gb300", "csrc")
     h = hashlib.sha256()
     for f in TRAFFIC_SOURCES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
-    if h.hexdigest()[:16] != TRAFFIC_SOURCES_SHA:
+        with open(os.path.join(csrc, f)) as fh:
+            lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in fh.read().split("\n")]
+        h.update(("\n".join(ln for ln in lines if ln.strip()) + "\n").encode())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(config: int):
+    if sources_sha() != TRAFFIC_SOURCES_SHA:
         return None
     return TRAFFIC_GATE_UP.get(config)
 
