@@ -277,6 +277,29 @@ def test_expert_row_counts_0_1_65(M):
     assert dl.get("counts").tolist() == [0, 1, 64, 65, 0, 129]
 
 
+SPLIT_COUNTS = [0, 1, 2, 7, 8, 9, 16, 17, 24, 25, 31, 32, 33, 64, 128, 160, 161, 300]
+
+
+@pytest.mark.parametrize("fmts", [(synth.W2, synth.W2), (synth.W4NL, synth.Q8_0)])
+def test_tile_split_row_counts(M, fmts):
+    """Row counts around every tile rule: small-row tiles of 1 to 4 n8
+    fragments (1..32 rows), the 32/33-row cutoff, a full 128-row tile alone,
+    with a 32-row small remainder (160), with a 33-row tcgen05 remainder
+    (161), and 2 full tiles + 44 (300)."""
+    k, E = 1, len(SPLIT_COUNTS)
+    ids = np.concatenate([np.full(c, e, np.int64) for e, c in enumerate(SPLIT_COUNTS)])
+    ids = np.random.default_rng(1).permutation(ids)
+    shape = synth.LayerShape(len(ids), 256, 128, E, k, *fmts)
+    L = _layer_with_ids(shape, ids)
+    o = oracle.layer(L)
+    for mode in ("layer", "stages"):
+        dl = DeviceLayer(M, L)
+        dl.run_layer() if mode == "layer" else dl.run_stages()
+        assert dl.status() == 0
+        assert dl.get("counts").tolist() == SPLIT_COUNTS
+        check_full(dl, o)
+
+
 def test_zero_and_huge_rows(M):
     """A zero token (every block d = 0, q = 0) and a token with one huge
     value (its block quantizes the rest to 0)."""
