@@ -218,12 +218,14 @@ def _layer_with_ids(shape, ids, seed=3, x_override=None):
     return L
 
 
-@pytest.mark.parametrize("T", [1638, 1639, 40000])
-def test_route_both_paths_bit_exact(M, T):
+@pytest.mark.parametrize("T,E", [(1638, 512), (1639, 512), (40000, 512), (1000, 1024),
+                                 (3000, 1024)])
+def test_route_both_paths_bit_exact(M, T, E):
     """Routing runs in one CTA up to 2^14 flat entries and in three kernels
     beyond; both give the oracle's counts, bounds, stable permutation and
-    largest-first order bit for bit (T*k = 16,380 / 16,390 / 400,000)."""
-    E, k = 512, 10
+    largest-first order bit for bit (T*k = 16,380 / 16,390 / 400,000, and
+    10,000 / 30,000 over the largest expert count, 1024)."""
+    k = 10
     rng = np.random.default_rng(T)
     ids_np, _ = synth.draw_topk_routing(rng, T, E, k, True)
     ids_np[7, 3] = E + 5  # one bad id: dropped and flagged
