@@ -157,24 +157,26 @@ int moe_workspace_view(const MoeLayerDesc *desc, void *workspace,
 /* Device-tiled weight pack.  The product kernels read the weights in a
  * tiled byte order, a permutation of the row-major pack made once per layer
  * (at load time) by moe_tile_weights.  For each weight matrix [N_out x K] of
- * bpr = K / (values per block) blocks per row:
+ * bpr = K / (values per block) blocks per row, BB bytes a block (18; 34 for
+ * Q8_0), CB code bytes a block (BB - 2) and cb blocks a chunk (4; 2 for
+ * Q8_0):
  *   tile t holds NW = min(256, N_out - 256t) rows and starts at byte
- *     256*t*bpr*18 of the matrix.  Down: rows 256t .. 256t+NW-1.  Gate/up:
+ *     256*t*bpr*BB of the matrix.  Down: rows 256t .. 256t+NW-1.  Gate/up:
  *     gate rows 128t .. 128t+NW/2-1, then the matching up rows (tile row
  *     r < NW/2 is gate output 128t+r, tile row NW/2+r is up output
  *     128t+r); gate output g is row g of the row-major matrix and up output
  *     g row n_ff+g (MOE_GU_SPLIT), or rows 2g and 2g+1 (MOE_GU_INTERLEAVED);
- *   chunk c of a tile covers blocks 4c .. 4c+nbc-1, nbc = min(4, bpr - 4c),
- *     and starts at byte 4*c*NW*18 of the tile;
- *   inside a chunk, the 16 code bytes (block bytes 2..17) of (tile row r,
- *     chunk block j) lie at (j*NW + r)*16, then the fp16 scales (block bytes
- *     0..1) at nbc*NW*16 + (j*NW + r)*2.
+ *   chunk c of a tile covers blocks cb*c .. cb*c+nbc-1, nbc = min(cb,
+ *     bpr - cb*c), and starts at byte cb*c*NW*BB of the tile;
+ *   inside a chunk, the CB code bytes (block bytes 2..BB-1) of (tile row r,
+ *     chunk block j) lie at (j*NW + r)*CB, then the fp16 scales (block bytes
+ *     0..1) at nbc*NW*CB + (j*NW + r)*2.
  * A tiled matrix has the row-major matrix's size.  Expert e's gate/up matrix
  * starts at e*(G + D) and its down matrix at e*(G + D) + G, G and D the
  * matrices' sizes; moe_tiled_pack_bytes(desc) = E*(G + D). */
 int64_t moe_tiled_pack_bytes(const MoeLayerDesc *desc);
 
-/* Tile a row-major weight pack (the layout of MOE_FMT_W2 / MOE_FMT_W4NL
+/* Tile a row-major weight pack (the block layouts of the MOE_FMT_* formats
  * above: expert e's gate/up matrix [2*n_ff x d] at expert_offsets[2e], its
  * down matrix [d x n_ff] at expert_offsets[2e+1], each offset a multiple of
  * 16 and each matrix inside weight_pack_bytes).
