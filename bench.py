@@ -101,6 +101,15 @@ def layer_bytes(L) -> dict:
     return parts
 
 
+def config_layer(args) -> synth.Layer:
+    """The seeded layer of --config, with --down-fmt / --gu-layout applied."""
+    fmt = {"w2": synth.W2, "w4nl": synth.W4NL, "q8_0": synth.Q8_0}
+    lay = {"split": synth.GU_SPLIT, "interleaved": synth.GU_INTERLEAVED}
+    return synth.config_layer(args.config,
+                              down_fmt=fmt[args.down_fmt] if args.down_fmt else None,
+                              gu_layout=lay[args.gu_layout] if args.gu_layout else None)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -212,7 +221,7 @@ def run_reference(args):
     world, rank, _ = dist_setup(args)
     if rank != 0:
         return 0
-    L = synth.config_layer(args.config)
+    L = config_layer(args)
     s = L.shape
     tok = args.ref_tokens
     for w in range(args.warmup):
@@ -253,7 +262,7 @@ def run_ours(args):
     if M.moe_check_device() != M.MOE_OK:
         raise SystemExit("current device is not an sm_103 GPU")
 
-    L = synth.config_layer(args.config)
+    L = config_layer(args)
     s = L.shape
     dev = f"cuda:{local}"
     x = torch.from_numpy(L.x).to(dev)
@@ -262,7 +271,8 @@ def run_ours(args):
     # weights: uploaded row-major, tiled once (load time, outside every timed region)
     desc, pack, eoff = M.tile_weights(s.T, s.d, s.n_ff, s.E, s.k, s.gu_fmt, s.down_fmt,
                                       torch.from_numpy(L.weight_pack).to(dev),
-                                      torch.from_numpy(L.expert_offsets).to(dev))
+                                      torch.from_numpy(L.expert_offsets).to(dev),
+                                      gu_layout=s.gu_layout)
     torch.cuda.synchronize()
     out = torch.empty((s.T, s.d), dtype=torch.float32, device=dev)
     ws = M.alloc_workspace(desc, dev)
@@ -358,7 +368,9 @@ def run_ours(args):
     alu_peak = SM_COUNT * FP32_LANES_PER_SM * sm_mhz * 1e6 / 1e12  # T lane-ops/s
     alu_achieved = 2.0 * pairs / (gu_ms * 1e-3) / 1e12
     eff_tops = value * s.k * ops_per_row(s) / 1e12
-    traffic = measured_traffic(args.config)
+    # the recorded traffic and algorithmic bytes are for the configuration as listed
+    variant = args.down_fmt is not None or args.gu_layout is not None
+    traffic = None if variant else measured_traffic(args.config)
     hbm = layer_bytes(L)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -367,7 +379,8 @@ def run_ours(args):
         "dtype": "int8 values in f16 MMA operands, f32 accumulate and epilogue",
         "data": "synthetic",
         "config": {"workload": L.name, "T": s.T, "d": s.d, "n_ff": s.n_ff, "E": s.E, "k": s.k,
-                   "gu_fmt": "W2", "down_fmt": "W2" if s.down_fmt == synth.W2 else "W4NL",
+                   "gu_fmt": synth.FMT_NAMES[s.gu_fmt], "down_fmt": synth.FMT_NAMES[s.down_fmt],
+                   "gu_layout": "interleaved" if s.gu_layout == synth.GU_INTERLEAVED else "split",
                    "seed": 1000 + args.config, "parallelism": f"replicas x{world}",
                    "l2": "no flush: every step streams > 3 GB (weights 0.71 GB, "
                          "intermediates > 2.5 GB) through a 129 MB L2"},
@@ -427,6 +440,10 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=2048)
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--down-fmt", choices=["w2", "w4nl", "q8_0"], default=None,
+                    help="the configuration with its down matrices in another format")
+    ap.add_argument("--gu-layout", choices=["split", "interleaved"], default=None,
+                    help="the configuration with its gate/up rows in another layout")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":

@@ -219,11 +219,22 @@ def make_layer(shape: LayerShape, seed: int, routing: str = "topk",
     return Layer(shape, x, ids, w, pack, offs, name)
 
 
-def config_layer(index: int) -> Layer:
-    """Seeded layer of configuration ``index`` (seed 1000 + index)."""
+FMT_NAMES = {W2: "W2", W4NL: "W4NL", Q8_0: "Q8_0"}
+
+
+def config_layer(index: int, down_fmt: int | None = None,
+                 gu_layout: int | None = None) -> Layer:
+    """Seeded layer of configuration ``index`` (seed 1000 + index), optionally
+    with another down format or gate/up row layout (named in ``name``)."""
     c = CONFIGS[index]
-    return make_layer(c["shape"], 1000 + index, c["routing"], c["bias"],
-                      c["outliers"], name=c["name"])
+    shape, name = c["shape"], c["name"]
+    if down_fmt is not None and down_fmt != shape.down_fmt:
+        shape = dataclasses.replace(shape, down_fmt=down_fmt)
+        name += "_down" + FMT_NAMES[down_fmt].lower()
+    if gu_layout is not None and gu_layout != shape.gu_layout:
+        shape = dataclasses.replace(shape, gu_layout=gu_layout)
+        name += "_gu_interleaved" if gu_layout == GU_INTERLEAVED else "_gu_split"
+    return make_layer(shape, 1000 + index, c["routing"], c["bias"], c["outliers"], name=name)
 
 
 def token_slice(layer: Layer, t0: int, t1: int) -> Layer:
