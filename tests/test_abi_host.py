@@ -112,3 +112,17 @@ def test_noalloc_route_rejects_sizes_beyond_its_scratch(lib):
     assert "scratch" in M.status_string(rc)
     d = M.make_desc(64, 256, 64, 8, 2)
     assert lib.moe_route_noalloc(ctypes.byref(d), fake, None, fake, fake, fake, None) == M.MOE_ERR_NULL
+
+
+@pytest.mark.parametrize("gu_fmt", [M.MOE_FMT_W2, M.MOE_FMT_W4NL, M.MOE_FMT_Q8_0])
+@pytest.mark.parametrize("down_fmt", [M.MOE_FMT_W2, M.MOE_FMT_W4NL, M.MOE_FMT_Q8_0])
+@pytest.mark.parametrize("layout", [M.MOE_GU_SPLIT, M.MOE_GU_INTERLEAVED])
+def test_every_format_and_layout_is_accepted(lib, gu_fmt, down_fmt, layout):
+    """Every weight format for either matrix and both gate/up layouts pass
+    validation, and the tiled pack is exactly the row-major matrices' bytes."""
+    import synth
+    T, d, n_ff, E, k = 64, 640, 320, 6, 2
+    desc = M.make_desc(T, d, n_ff, E, k, gu_fmt, down_fmt, 0, layout)
+    assert lib.moe_prefill_workspace_bytes(ctypes.byref(desc)) > 0
+    want = E * (2 * n_ff * synth.row_bytes(gu_fmt, d) + d * synth.row_bytes(down_fmt, n_ff))
+    assert M.tiled_pack_bytes(desc) == want
