@@ -45,8 +45,8 @@ INT8_MMA_PEAK_TOPS = 150.0
 # DRAM bytes of one gate/up stage (the tcgen05 launch plus the small-row
 # launch) at configuration 2 (ncu, one pass: profiles/dram_gate_up_T16384.md),
 # valid while the product kernels' sources hash as they did at capture
-TRAFFIC_GATE_UP = {2: 1.5877e9}
-TRAFFIC_SOURCES_SHA = "0c5a7146ca560c87"
+TRAFFIC_GATE_UP = {2: 1.5878e9}
+TRAFFIC_SOURCES_SHA = "ebb456ec0ce2dcac"
 TRAFFIC_SOURCES = ("gemm_tc.cu", "gemm_small.cu", "route.cu", "sm100_ptx.cuh", "common.cuh")
 ALGO_BYTES_GATE_UP = {2: 1.586e9}
 

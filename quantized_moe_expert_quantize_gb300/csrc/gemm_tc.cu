@@ -484,9 +484,13 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
               const float* dws = sDw + (gb % kDwRing) * kTN + (taddr & 0xFFFFu) - (buf * kTN) -
                                  (uint32_t)(tmem & 0xFFFFu);
 #pragma unroll
-              for (int j = 0; j < 8; j++) {
-                const float2 w2 = *reinterpret_cast<const float2*>(dws + 2 * j);
-                acc[8 * c + j] = __ffma2_rn(__fmul2_rn(w2, dx2), v[j], acc[8 * c + j]);
+              for (int j = 0; j < 4; j++) {
+                // 16-byte loads: the 16 columns start 64-byte aligned
+                const float4 w4 = *reinterpret_cast<const float4*>(dws + 4 * j);
+                acc[8 * c + 2 * j] = __ffma2_rn(__fmul2_rn(make_float2(w4.x, w4.y), dx2),
+                                                v[2 * j], acc[8 * c + 2 * j]);
+                acc[8 * c + 2 * j + 1] = __ffma2_rn(__fmul2_rn(make_float2(w4.z, w4.w), dx2),
+                                                    v[2 * j + 1], acc[8 * c + 2 * j + 1]);
               }
             }
           }
