@@ -25,8 +25,13 @@
  * Conventions for every entry point:
  *   - Every pointer argument named d_* or documented "device" is device
  *     memory of the current CUDA device, owned by the caller.  The library
- *     allocates nothing and keeps no state between calls except a launch
- *     counter; all work is enqueued on `stream` with no host
+ *     allocates no device memory and keeps no state between calls except a
+ *     launch counter and, per device, one CUDA stream and two events
+ *     (created on the first product call that is not being captured, kept
+ *     until the process exits): the products' small-row launch runs on that
+ *     stream, forked from `stream` by an event and joined back before the
+ *     call returns, so the work stays ordered on `stream` (under stream
+ *     capture, as graph edges).  All work is enqueued with no host
  *     synchronisation, unless the entry point says otherwise.
  *   - Arguments are validated on the host before anything is launched; a
  *     negative MOE_ERR_* code is returned and nothing is enqueued.
