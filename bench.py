@@ -464,6 +464,10 @@ def run_ours(args):
 
 
 def main():
+    return main_args(sys.argv[1:])
+
+
+def main_args(argv):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
@@ -480,7 +484,7 @@ def main():
                     help="the configuration with its down matrices in another format")
     ap.add_argument("--gu-layout", choices=["split", "interleaved"], default=None,
                     help="the configuration with its gate/up rows in another layout")
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":
         return run_reference(args)
