@@ -302,6 +302,52 @@ def test_tile_split_row_counts(M, fmts):
         check_full(dl, o)
 
 
+def _two_expert_ids(T: int) -> np.ndarray:
+    """k = 2 over 3 experts: every token routes to expert 0 and to expert 1
+    (tokens < T - 3) or 2 (the last 3), ranks in a seeded order.  Counts
+    [T, T - 3, 3]: for T = 132, a full 128-row tile plus a 4-row remainder,
+    a full tile plus a 1-row remainder, and a 3-row small tile."""
+    rng = np.random.default_rng(11)
+    ids = np.zeros((T, 2), np.int64)
+    ids[:, 1] = 1
+    ids[T - 3:, 1] = 2
+    swap = rng.random(T) < 0.5
+    ids[swap] = ids[swap][:, ::-1]
+    return ids.reshape(-1)
+
+
+EXTREME = {
+    # the largest d (gate/up K = 8192, 256 blocks in the epilogue; down
+    # output 8192 rows = 32 weight tiles) with the smallest n_ff
+    "d8192_nff64_w2_w2": (synth.LayerShape(132, 8192, 64, 3, 2, synth.W2, synth.W2), "two"),
+    # the largest n_ff (down K = 4096, gate/up output 8192 rows) with the
+    # smallest d (gate/up K = 128: two W2 or four W4NL blocks a row)
+    "d128_nff4096_w4nl_q8": (synth.LayerShape(132, 128, 4096, 3, 2, synth.W4NL, synth.Q8_0), "two"),
+    "d128_nff4096_w2_w2_inter": (synth.LayerShape(132, 128, 4096, 3, 2, synth.W2, synth.W2,
+                                                  synth.GU_INTERLEAVED), "two"),
+    # the largest E, most experts with 0-3 rows
+    "E1024_w2_w4nl": (synth.LayerShape(300, 128, 64, 1024, 4, synth.W2, synth.W4NL), "topk"),
+}
+
+
+@pytest.mark.parametrize("name", list(EXTREME))
+def test_extreme_shapes(M, name):
+    """The ends of the supported shape range (d 128 and 8192, n_ff 64 and
+    4096, E 1024), every stage against the oracle, as one layer call and as
+    stages."""
+    shape, routing = EXTREME[name]
+    if routing == "two":
+        L = _layer_with_ids(shape, _two_expert_ids(shape.T))
+    else:
+        L = synth.make_layer(shape, seed=12, routing="topk", bias=True, outliers=True)
+    o = oracle.layer(L)
+    for mode in ("layer", "stages"):
+        dl = DeviceLayer(M, L)
+        dl.run_layer() if mode == "layer" else dl.run_stages()
+        assert dl.status() == 0
+        check_full(dl, o)
+
+
 def test_zero_and_huge_rows(M):
     """A zero token (every block d = 0, q = 0) and a token with one huge
     value (its block quantizes the rest to 0)."""
