@@ -37,6 +37,15 @@ MUTANTS = [
     ("combine_reverse", "for (int r = 0; r < k; r++) {\n        int32_t pos = dst_of[t * k + r];",
      "for (int r = k - 1; r >= 0; r--) {\n        int32_t pos = dst_of[t * k + r];"),
     ("combine_weight_index", "fmaf(w[t * k + r]", "fmaf(w[t * k]"),
+    ("interleaved_swapped", "g = gu[2 * j];\n      u = gu[2 * j + 1];",
+     "g = gu[2 * j + 1];\n      u = gu[2 * j];"),
+    ("scale_big_endian", "blk[0] | (blk[1] << 8)", "blk[1] | (blk[0] << 8)"),
+    ("half_subnormal_exponent", "ldexpf((float)man, -24)", "ldexpf((float)man, -25)"),
+    ("nl4_table_entry", "1,    13,   25,  38,  53,  69,  89,  113}",
+     "1,    13,   25,  38,  53,  69,  89,  112}"),
+    ("layer_token_of_row", "int64_t t = src / j->k;", "int64_t t = src % j->k;"),
+    ("layer_down_offset", "j->eoff[2 * e + 1]", "j->eoff[2 * e]"),
+    ("layer_expert_of_row", "int e = j->ids[src];", "int e = j->ids[r];"),
 ]
 
 
