@@ -102,3 +102,13 @@ def test_sources_sha_ignores_comments(tmp_path, monkeypatch):
     assert bench.sources_sha() == h0
     (csrc / bench.TRAFFIC_SOURCES[0]).write_text("int a;\nint c;\n")
     assert bench.sources_sha() != h0
+
+
+def test_l2_note_follows_the_step_footprint():
+    """The bench's L2 statement: a layer step that touches more than twice the
+    L2 streams through it; a tiny one says it is timed L2-warm."""
+    import bench
+    big = bench.l2_note(bench.layer_bytes(synth.config_layer(4)))
+    assert big.startswith("no flush: every step touches") and "GB" in big
+    small = bench.l2_note(bench.layer_bytes(synth.config_layer(0)))
+    assert "L2-warm" in small
