@@ -328,9 +328,10 @@ class Layer:
     pack) plus its workspace, for repeated calls at a fixed token count."""
 
     def __init__(self, T, d, n_ff, E, k, gu_fmt, down_fmt, weight_pack: torch.Tensor,
-                 expert_offsets: torch.Tensor, device="cuda"):
+                 expert_offsets: torch.Tensor, device="cuda", gu_layout=MOE_GU_SPLIT):
         self.desc, self.weight_pack, self.expert_offsets = tile_weights(
-            T, d, n_ff, E, k, gu_fmt, down_fmt, weight_pack, expert_offsets)
+            T, d, n_ff, E, k, gu_fmt, down_fmt, weight_pack, expert_offsets,
+            gu_layout=gu_layout)
         self.workspace = alloc_workspace(self.desc, device)
 
     def __call__(self, x, topk_ids, topk_w, out=None, stream=None):

@@ -489,3 +489,19 @@ def test_smoke_entry_point(M):
     oracle (tiled weights, routed-row q8, Hq and out tolerances)."""
     import __graft_entry__
     __graft_entry__.smoke()
+
+
+def test_layer_class_equals_device_entry(M):
+    """The binding's Layer (weights tiled when it is built, workspace kept)
+    gives the device entry point's output bit for bit."""
+    L = SMALL["mid_w4nl_w2_inter"]()
+    s = L.shape
+    dl = DeviceLayer(M, L)
+    dl.run_layer()
+    layer = M.Layer(s.T, s.d, s.n_ff, s.E, s.k, s.gu_fmt, s.down_fmt,
+                    torch.from_numpy(L.weight_pack).cuda(),
+                    torch.from_numpy(L.expert_offsets).cuda(), gu_layout=s.gu_layout)
+    out = layer(dl.x, dl.ids, dl.w)
+    torch.cuda.synchronize()
+    assert torch.equal(out, dl.out)
+    assert layer.status() == 0
