@@ -505,3 +505,51 @@ def test_layer_class_equals_device_entry(M):
     torch.cuda.synchronize()
     assert torch.equal(out, dl.out)
     assert layer.status() == 0
+
+
+def _unit_scales_and_extremes(L: synth.Layer, n_extreme: int, rng) -> None:
+    """Every weight block scale set to fp16 1.0, the first ``n_extreme`` rows
+    of every gate/up matrix set to the format's most negative code (W2 c = 0,
+    value -2; W4NL index 0, value -127; Q8_0 -127), and x to integers in
+    [-127, 127] whose every 32-value block holds a +-127 (so d_x = 1)."""
+    s = L.shape
+    for e in range(s.E):
+        for m, (fmt, rows, K) in enumerate(((s.gu_fmt, 2 * s.n_ff, s.d),
+                                            (s.down_fmt, s.d, s.n_ff))):
+            bb = synth.BLOCK_BYTES_OF[fmt]
+            nb = K // synth.BLOCK_VALUES[fmt]
+            o = int(L.expert_offsets[e, m])
+            mat = L.weight_pack[o:o + rows * nb * bb].reshape(rows, nb, bb)
+            mat[:, :, 0] = 0x00
+            mat[:, :, 1] = 0x3C
+            if m == 0:
+                mat[:n_extreme, :, 2:] = 0x81 if fmt == synth.Q8_0 else 0x00
+    x = rng.integers(-127, 128, size=(s.T, s.d)).astype(np.float32)
+    x[:, ::32] = np.where(rng.random((s.T, s.d // 32)) < 0.5, -127.0, 127.0)
+    x[:10] = -127.0
+    L.x = x
+
+
+@pytest.mark.parametrize("fmts", [(synth.W2, synth.W2), (synth.W4NL, synth.Q8_0),
+                                  (synth.Q8_0, synth.W4NL)])
+def test_block_sums_exact_at_extremes(M, fmts):
+    """The block sums are exact on both tensor-core paths: with every scale
+    1.0 (d_w = d_x = 1) GU is the K-ordered fp32 sum of the integer block
+    sums on both sides, so it must equal the oracle bit for bit, including
+    blocks at the integer extremes (|isum| = 8,128 for W2 and 516,128 for
+    W4NL and Q8_0).  Row counts put tiles on both product kernels."""
+    counts = [129, 31, 160, 5]
+    ids = np.random.default_rng(5).permutation(
+        np.concatenate([np.full(c, e, np.int64) for e, c in enumerate(counts)]))
+    shape = synth.LayerShape(len(ids), 512, 128, len(counts), 1, *fmts)
+    L = _layer_with_ids(shape, ids)
+    _unit_scales_and_extremes(L, 16, np.random.default_rng(6))
+    o = oracle.layer(L)
+    dl = DeviceLayer(M, L)
+    dl.run_stages()
+    assert dl.status() == 0
+    check_route(dl, o)
+    check_q8_x(dl, o)
+    R = int(o["offsets"][-1])
+    gu = dl.get("gu", R)
+    assert np.array_equal(gu, o["gu"]), float(np.max(np.abs(gu - o["gu"])))
