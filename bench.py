@@ -33,12 +33,12 @@ import synth  # noqa: E402
 
 METRIC = "MoE-layer prefill tokens/s and effective int8 TOPS at 16K tokens, top-10"
 UNIT = "tokens/s"
-# peaks: MEASURED_PEAKS.json when the driver wrote it, else these fallbacks
+# peaks: MEASURED_PEAKS.json when present, else these fallbacks
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 SM_COUNT = 152
 FP32_LANES_PER_SM = 128
-# sm_103a's int8 tensor peak: mma.sync.m16n8k32.s8 measured on this machine's
+# sm_103a's int8 tensor peak: mma.sync.m16n8k32.s8 as measured on a
 # GB300 (tcgen05 kind::i8 does not exist there); MEASURED_PEAKS.json has no
 # int8 figure
 INT8_MMA_PEAK_TOPS = 150.0
