@@ -262,6 +262,10 @@ def check_combine(seed=5):
     dm = np.array(g["dm_rows"], np.float32)
     out = oracle.combine(w, np.arange(3, dtype=np.int32), dm, 1)
     assert out[0, 0] == np.float32(g["expect_rank_order"]), out
+    f = g["fma"]
+    out = oracle.combine(np.array(f["topk_w"], np.float32), np.arange(2, dtype=np.int32),
+                         np.array(f["dm_rows"], np.float32), 1)
+    assert out[0, 0] == np.float32(f["expect"]), (f["why"], out[0, 0])
     rng = np.random.default_rng(seed)
     T, k, d = 9, 4, 64
     R = T * k

@@ -46,6 +46,11 @@ MUTANTS = [
     ("layer_token_of_row", "int64_t t = src / j->k;", "int64_t t = src % j->k;"),
     ("layer_down_offset", "j->eoff[2 * e + 1]", "j->eoff[2 * e]"),
     ("layer_expert_of_row", "int e = j->ids[src];", "int e = j->ids[r];"),
+    # rounding-level mistakes: each against a hand example where it changes a bit
+    ("q8_reciprocal", "rintf(xb[i] / db)", "rintf(xb[i] * (1.0f / db))"),
+    ("epilogue_unfused", "acc = fmaf(s, (float)isum, acc);", "acc = acc + s * (float)isum;"),
+    ("combine_unfused", "acc = fmaf(w[t * k + r], dm[(int64_t)pos * d + j], acc);",
+     "acc = acc + w[t * k + r] * dm[(int64_t)pos * d + j];"),
 ]
 
 
