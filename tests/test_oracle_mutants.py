@@ -46,6 +46,14 @@ MUTANTS = [
     ("layer_token_of_row", "int64_t t = src / j->k;", "int64_t t = src % j->k;"),
     ("layer_down_offset", "j->eoff[2 * e + 1]", "j->eoff[2 * e]"),
     ("layer_expert_of_row", "int e = j->ids[src];", "int e = j->ids[r];"),
+    ("w2_scale_per_32", "const uint8_t *blk = row + (int64_t)(j / bv) * orc_block_bytes(fmt);\n  return orc_half",
+     "const uint8_t *blk = row + (int64_t)(j / 32) * orc_block_bytes(fmt);\n  return orc_half"),
+    ("q8_scale_fp16", "    d[b] = db;", "    d[b] = (float)(_Float16)db;"),
+    ("q8_signed_amax", "float a = fabsf(xb[i]);", "float a = xb[i];"),
+    ("product_q_unsigned", "isum += wi[32 * b + i] * (int32_t)q[32 * b + i];",
+     "isum += wi[32 * b + i] * (int32_t)(uint8_t)q[32 * b + i];"),
+    ("route_bad_id_to_row_0", "      dst_of[i] = -1;", "      dst_of[i] = 0;"),
+    ("swiglu_scale_row", "dh + r * (n_ff / 32), h);", "dh + r * (n_ff / 32 - 1), h);"),
     # rounding-level mistakes: each against a hand example where it changes a bit
     ("q8_reciprocal", "rintf(xb[i] / db)", "rintf(xb[i] * (1.0f / db))"),
     ("epilogue_unfused", "acc = fmaf(s, (float)isum, acc);", "acc = acc + s * (float)isum;"),
