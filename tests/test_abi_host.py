@@ -126,3 +126,31 @@ def test_every_format_and_layout_is_accepted(lib, gu_fmt, down_fmt, layout):
     assert lib.moe_prefill_workspace_bytes(ctypes.byref(desc)) > 0
     want = E * (2 * n_ff * synth.row_bytes(gu_fmt, d) + d * synth.row_bytes(down_fmt, n_ff))
     assert M.tiled_pack_bytes(desc) == want
+
+
+def test_plain_c_consumer(lib, tmp_path):
+    """The boundary is a C ABI: a C99 program that includes only the header
+    compiles warning-free, links the library, and gets from the host-side
+    entry points what the Python binding gets."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    exe = tmp_path / "consumer"
+    pkg = os.path.dirname(M.LIB_PATH)
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                    "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "c_abi_consumer.c"),
+                    "-L", pkg, "-lmoeprefill", f"-Wl,-rpath,{pkg}", "-o", str(exe)],
+                   check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split(" ", 6)
+    d = M.make_desc(16384, 2560, 640, 512, 10, M.MOE_FMT_W2, M.MOE_FMT_W4NL, 0,
+                    M.MOE_GU_INTERLEAVED)
+    assert int(out[0]) == M.workspace_bytes(d)
+    assert int(out[1]) == M.tiled_pack_bytes(d)
+    assert int(out[2]) == M.host_io_bytes(d)
+    assert int(out[3]) == 0
+    assert int(out[4]) == M.MOE_ERR_NULL
+    assert int(out[5]) == M.MOE_ERR_SHAPE
+    assert out[6].strip() == M.status_string(M.MOE_ERR_SHAPE)
