@@ -487,9 +487,6 @@ def main_args(argv):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--stage-steps", type=int, default=20,
-                    help="no effect (stage times now come from the timed steps); accepted so "
-                         "older command lines still run")
     ap.add_argument("--cpu-tokens", type=int, default=2048)
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
