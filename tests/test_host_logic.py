@@ -112,3 +112,16 @@ def test_l2_note_follows_the_step_footprint():
     assert big.startswith("no flush: every step touches") and "GB" in big
     small = bench.l2_note(bench.layer_bytes(synth.config_layer(0)))
     assert "L2-warm" in small
+
+
+def test_oracle_layer_does_not_depend_on_its_thread_count():
+    """The oracle splits routed rows over threads; each row's arithmetic is
+    fixed, so every output is the same bits for 1, 3 and 8 threads."""
+    import oracle
+    L = synth.make_layer(synth.LayerShape(40, 256, 64, 6, 3, synth.W4NL, synth.W2), seed=31,
+                         routing="topk", bias=True, outliers=True)
+    runs = [oracle.layer(L, threads=t) for t in (1, 3, 8)]
+    for o in runs[1:]:
+        for key, v in runs[0].items():
+            if key != "threads":
+                assert np.array_equal(np.asarray(v), np.asarray(o[key])), key
