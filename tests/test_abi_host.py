@@ -154,3 +154,31 @@ def test_plain_c_consumer(lib, tmp_path):
     assert int(out[4]) == M.MOE_ERR_NULL
     assert int(out[5]) == M.MOE_ERR_SHAPE
     assert out[6].strip() == M.status_string(M.MOE_ERR_SHAPE)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """No fallback: with the library absent, the binding raises instead of
+    computing anything."""
+    monkeypatch.setattr(M, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(M, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        M.lib()
+    d = M.make_desc(8, 256, 64, 4, 2)
+    with pytest.raises(RuntimeError):
+        M.workspace_bytes(d)
+
+
+def test_product_code_never_touches_the_oracle():
+    """The package and the library sources neither import, include, load nor
+    call the oracle: it is test infrastructure only."""
+    pkg = os.path.join(ROOT, "quantized_moe_expert_quantize_gb300")
+    uses = re.compile(r"^\s*(import|from)\s+oracle\b|#\s*include\s*[<\"][^>\"]*oracle"
+                      r"|liboracle|moe_oracle|\borc_\w+\s*\(", re.M)
+    paths = [os.path.join(d, f) for d, _, fs in os.walk(pkg) for f in fs]
+    paths += [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))]
+    checked = 0
+    for path in paths:
+        if path.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+            assert not uses.search(open(path).read()), path
+            checked += 1
+    assert checked >= 10
