@@ -182,3 +182,17 @@ def test_product_code_never_touches_the_oracle():
             assert not uses.search(open(path).read()), path
             checked += 1
     assert checked >= 10
+
+
+def test_oracle_never_touches_the_cuda_path():
+    """The oracle neither imports the package nor loads or includes the CUDA
+    library: the two sides share only the seeded inputs."""
+    uses = re.compile(r"^\s*(import|from)\s+quantized_moe_expert_quantize_gb300|libmoeprefill"
+                      r"|#\s*include\s*[<\"][^>\"]*(moe_prefill\.h|\.cuh)|\bmoe_\w+\s*\(", re.M)
+    odir = os.path.join(ROOT, "oracle")
+    checked = 0
+    for fn in os.listdir(odir):
+        if fn.endswith((".py", ".c", ".h")):
+            assert not uses.search(open(os.path.join(odir, fn)).read()), fn
+            checked += 1
+    assert checked >= 3
