@@ -297,6 +297,18 @@ int moe_route_noalloc(const MoeLayerDesc *desc, const int32_t *topk_ids,
                       int32_t *counts, int32_t *offsets, int32_t *row_src,
                       int32_t *dst_of, moe_stream_t stream);
 
+/* Self-test of the failure path of the bounded pipeline waits (tests only).
+ * Enqueues one warp that waits on an mbarrier nothing ever completes,
+ * through the wait routine the product kernels use: sleep = 1 takes the
+ * timed wait of the producer and decode roles (gives up after 20 ms of
+ * global time), sleep = 0 the polling wait of the epilogue and MMA roles
+ * (gives up after its fixed count of polls, about 1.4 s on a GB300).  On
+ * giving up it or-s MOE_STATUS_PIPE_TIMEOUT into *status (device int32,
+ * 4-byte aligned) and exits; nothing faults or traps and the context stays
+ * usable.  Returns MOE_OK once enqueued, MOE_ERR_NULL / MOE_ERR_ALIGN /
+ * MOE_ERR_SHAPE (sleep not 0 or 1) / MOE_ERR_DEVICE before enqueueing. */
+int moe_selftest_wait_timeout(int32_t *status, int sleep, moe_stream_t stream);
+
 /* MOE_OK when the current CUDA device is an sm_103 part, else MOE_ERR_DEVICE. */
 int moe_check_device(void);
 

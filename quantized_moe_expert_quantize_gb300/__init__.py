@@ -45,6 +45,7 @@ EXPORTS = (
     "moe_gate_up", "moe_swiglu_quant", "moe_down", "moe_combine", "moe_read_status",
     "moe_check_device", "moe_status_string", "moe_kernel_launches", "moe_route_noalloc",
     "moe_tiled_pack_bytes", "moe_tile_weights", "moe_gate_up_swiglu",
+    "moe_selftest_wait_timeout",
 )
 
 
@@ -122,6 +123,8 @@ def lib(build_if_missing: bool = False) -> ctypes.CDLL:
         L.moe_tiled_pack_bytes.restype = ctypes.c_int64
         L.moe_tile_weights.argtypes = [dp, vp, ctypes.c_int64, vp, vp, vp, vp, vp]
         L.moe_tile_weights.restype = i32
+        L.moe_selftest_wait_timeout.argtypes = [vp, i32, vp]
+        L.moe_selftest_wait_timeout.restype = i32
         L.moe_kernel_launches.argtypes = []
         L.moe_kernel_launches.restype = ctypes.c_uint64
         _lib = L
@@ -313,6 +316,13 @@ def moe_read_status(desc, workspace, stream=None) -> int:
     if rc not in (MOE_OK, MOE_ERR_DEVICE_STATUS):
         raise MoeError(rc, "moe_read_status")
     return int(st.value)
+
+
+def moe_selftest_wait_timeout(status, sleep: int, stream=None):
+    """Enqueue the bounded-wait self-test: a wait nothing completes must
+    give up and or MOE_STATUS_PIPE_TIMEOUT into ``status`` (device int32)."""
+    _check(lib().moe_selftest_wait_timeout(_ptr(status, torch.int32), int(sleep),
+                                           _stream(stream)), "moe_selftest_wait_timeout")
 
 
 def moe_check_device() -> int:

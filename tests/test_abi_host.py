@@ -196,3 +196,11 @@ def test_oracle_never_touches_the_cuda_path():
             assert not uses.search(open(os.path.join(odir, fn)).read()), fn
             checked += 1
     assert checked >= 3
+
+
+def test_wait_selftest_validates_before_enqueueing(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.moe_selftest_wait_timeout(None, 1, None) == M.MOE_ERR_NULL
+    assert lib.moe_selftest_wait_timeout(ctypes.c_void_p((1 << 20) + 2), 1, None) == M.MOE_ERR_ALIGN
+    assert lib.moe_selftest_wait_timeout(fake, 2, None) == M.MOE_ERR_SHAPE
+    assert lib.moe_selftest_wait_timeout(fake, 1, None) == M.MOE_ERR_DEVICE   # no GPU here

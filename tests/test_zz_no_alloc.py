@@ -5,8 +5,8 @@ instead of a caller workspace, for code that may only touch the buffers it
 is given.  Its outputs must equal those of moe_route (which uses a
 workspace) bit for bit -- routing is integer work -- on two calls in a row,
 the second on a different routing, since every call reuses the same array.
-This file is collected last so that a run stopping at the first failure has
-already run every other test.
+This file is collected near the end (before only the wait self-test), so
+that a run stopping at the first failure has already run the parity tests.
 """
 import numpy as np
 import pytest
