@@ -110,7 +110,10 @@ double orc_w_value(int fmt, const uint8_t *row, int j) {
 }
 
 /* ---------------------------------------------------------------- route */
-/* Returns the number of entries whose expert id is out of range; those get
+/* Histogram, exclusive prefix sum (group bounds) and stable bucketing of the
+ * T*k flat rows ("Strata #3752", commits "moe_ws wiring" and "swiglu_quant
+ * landed": quantize_scatter and the group bounds).
+ * Returns the number of entries whose expert id is out of range; those get
  * dst_of = -1 and no row. */
 int64_t orc_route(int64_t T, int k, int E, const int32_t *ids, int32_t *counts,
                   int32_t *offsets, int32_t *row_src, int32_t *dst_of) {
@@ -143,6 +146,9 @@ int64_t orc_route(int64_t T, int k, int E, const int32_t *ids, int32_t *counts,
 }
 
 /* ------------------------------------------------------------------- q8 */
+/* q8 of one row, block by block: amax, d = amax/127, q = rint(x/d), d = 0
+ * gives q = 0 (the layer spec's tiny configuration; "Strata #3752", commit
+ * "swiglu_quant": quantize_mmq_q8_1 on 32-value blocks). */
 static void orc_q8_row(int K, const float *x, int8_t *q, float *d) {
   for (int b = 0; b < K / 32; b++) {
     const float *xb = x + 32 * b;
@@ -164,7 +170,9 @@ void orc_quant_q8(int64_t rows, int K, const float *x, int8_t *q, float *d) {
 }
 
 /* ------------------------------------------------------------- products */
-/* One activation row (q, dq) against every row of one expert's weight
+/* The per-32-value epilogue in K order ("Strata #3752", commit "moe_ws
+ * kernels"): acc = fma(d_w*d_x, isum, acc) block by block, isum exact.
+ * One activation row (q, dq) against every row of one expert's weight
  * matrix [n_out x K]. */
 static void orc_product_row(int fmt, int K, int n_out, const uint8_t *wmat,
                             const int8_t *q, const float *dq, float *out) {
@@ -213,6 +221,8 @@ void orc_expert_rows(int fmt, int K, int n_out, const uint8_t *wmat,
 #define ORC_GU_SPLIT 0
 #define ORC_GU_INTERLEAVED 1
 
+/* H = silu(g)*u then q8 of H, H never kept beyond this row's scratch
+ * ("Strata #3752", commit "swiglu_quant"). */
 static void orc_swiglu_quant_row(int n_ff, int layout, const float *gu,
                                  int8_t *hq, float *dh, float *hbuf) {
   for (int j = 0; j < n_ff; j++) {
@@ -237,6 +247,9 @@ void orc_swiglu_quant(int64_t rows, int n_ff, int layout, const float *gu,
 }
 
 /* --------------------------------------------------------------- combine */
+/* out[t] = sum over ranks r = 0..k-1, in that order, of w[t,r]*Dm[row(t,r)],
+ * one fma per rank (the layer spec's tiny configuration); dropped rows add
+ * nothing. */
 void orc_combine(int64_t T, int k, int d, const float *w, const int32_t *dst_of,
                  const float *dm, float *out) {
   for (int64_t t = 0; t < T; t++)
