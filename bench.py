@@ -36,19 +36,21 @@ UNIT = "tokens/s"
 # peaks: MEASURED_PEAKS.json when present, else these fallbacks
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-SM_COUNT = 152
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 FP32_LANES_PER_SM = 128
 # sm_103a's int8 tensor peak: mma.sync.m16n8k32.s8 as measured on a
 # GB300 (tcgen05 kind::i8 does not exist there); MEASURED_PEAKS.json has no
 # int8 figure
 INT8_MMA_PEAK_TOPS = 150.0
-# DRAM bytes of one gate/up stage (the tcgen05 launch plus the small-row
-# launch) at configuration 2 (ncu, one pass: profiles/dram_gate_up_T16384.md),
-# valid while the product kernels' sources hash as they did at capture
+# DRAM bytes (read + write) of one gate/up stage -- the tcgen05 launch plus
+# the small-row launch -- at the 16,384-token layer, from a one-pass ncu
+# capture (dram__bytes_read.sum + dram__bytes_write.sum); reported while the
+# product kernels' code hashes as it did at that capture, else null
 TRAFFIC_GATE_UP = {2: 1.5878e9}
 TRAFFIC_SOURCES_SHA = "ebb456ec0ce2dcac"
 TRAFFIC_SOURCES = ("gemm_tc.cu", "gemm_small.cu", "route.cu", "sm100_ptx.cuh", "common.cuh")
 ALGO_BYTES_GATE_UP = {2: 1.586e9}
+OTHER_CONFIGS = (1, 3, 4)
 
 
 def sources_sha() -> str:
@@ -67,9 +69,15 @@ def sources_sha() -> str:
 
 
 def measured_traffic(config: int):
-    if sources_sha() != TRAFFIC_SOURCES_SHA:
-        return None
-    return TRAFFIC_GATE_UP.get(config)
+    """(bytes, source) of the recorded capture, or (None, why not)."""
+    sha = sources_sha()
+    if sha != TRAFFIC_SOURCES_SHA:
+        return None, (f"no capture of the current kernels (code hash {sha}; the last "
+                      f"capture was of {TRAFFIC_SOURCES_SHA})")
+    if config not in TRAFFIC_GATE_UP:
+        return None, f"no capture of configuration {config}"
+    return TRAFFIC_GATE_UP[config], (f"ncu dram__bytes_read.sum + dram__bytes_write.sum, one "
+                                     f"pass, kernel code hash {TRAFFIC_SOURCES_SHA}")
 
 
 def ops_per_row(s: synth.LayerShape) -> int:
@@ -164,7 +172,25 @@ def load_peaks():
                                                j.get("bf16_tflops", FALLBACK_BF16_TFLOPS))),
                     source="measured")
     return dict(hbm=FALLBACK_HBM_GBS, bf16=FALLBACK_BF16_TFLOPS,
-                bf16_sustained=FALLBACK_BF16_TFLOPS, source="fallback")
+                bf16_sustained=FALLBACK_BF16_TFLOPS_SUSTAINED, source="fallback")
+
+
+def tensor_peak(peaks: dict, clk: dict | None):
+    """The bf16 denominator for a product stage timed inside the layer's
+    steps: the burst figure when the clock record of the timed region shows
+    the SM clock at its maximum with no power-cap or thermal reason (the
+    burst figure's conditions), else the sustained one."""
+    clk = clk or {}
+    sm, smax, reasons = clk.get("sm_mhz"), clk.get("sm_max_mhz"), clk.get("reasons") or []
+    burst = (sm is not None and smax and sm >= 0.97 * smax and
+             not any(r in reasons for r in ("sw_power_cap", "hw_slowdown", "hw_thermal_slowdown",
+                                             "sw_thermal_slowdown")))
+    if burst:
+        return peaks["bf16"], (f"{peaks['source']} bf16 dense, burst: the timed region ran at "
+                               f"{sm:.0f} of {smax:.0f} MHz with no throttle reason")
+    return peaks["bf16_sustained"], (f"{peaks['source']} bf16 dense, sustained: the clock record "
+                                     f"of the timed region ({sm} of {smax} MHz, reasons "
+                                     f"{reasons}) is not the burst figure's")
 
 
 # ------------------------------------------------------------------ clocks
@@ -293,6 +319,115 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------ GPU arm
+class DeviceLayer:
+    """One seeded layer resident on the GPU: inputs, the tiled weight pack
+    (tiled once at load time, outside every timed region), out, workspace."""
+
+    def __init__(self, M, L: synth.Layer, dev: str):
+        import torch
+        s = L.shape
+        self.L, self.M = L, M
+        self.x = torch.from_numpy(L.x).to(dev)
+        self.ids = torch.from_numpy(L.topk_ids).to(dev)
+        self.w = torch.from_numpy(L.topk_w).to(dev)
+        raw = torch.from_numpy(L.weight_pack).to(dev)
+        roff = torch.from_numpy(L.expert_offsets).to(dev)
+        self.desc, self.pack, self.eoff = M.tile_weights(s.T, s.d, s.n_ff, s.E, s.k, s.gu_fmt,
+                                                         s.down_fmt, raw, roff,
+                                                         gu_layout=s.gu_layout)
+        torch.cuda.synchronize()
+        del raw, roff
+        self.out = torch.empty((s.T, s.d), dtype=torch.float32, device=dev)
+        self.ws = M.alloc_workspace(self.desc, dev)
+
+    def layer(self, stream=None):
+        self.M.moe_prefill_layer(self.desc, self.x, self.ids, self.w, self.pack, self.eoff,
+                                 self.out, self.ws, stream)
+
+    def stage_calls(self, stream):
+        """moe_prefill_layer's own launch sequence, one stage entry point each."""
+        M, d = self.M, self.desc
+        return [("route", lambda: M.moe_route(d, self.ids, self.ws, stream)),
+                ("quant_q8", lambda: M.moe_quant_q8(d, self.x, self.ws, stream)),
+                ("gate_up_swiglu",
+                 lambda: M.moe_gate_up_swiglu(d, self.pack, self.eoff, self.ws, stream)),
+                ("down", lambda: M.moe_down(d, self.pack, self.eoff, self.ws, stream)),
+                ("combine", lambda: M.moe_combine(d, self.w, self.out, self.ws, stream))]
+
+
+def time_stages(calls, steps: int, stream) -> dict:
+    """`steps` layers as their stage sequence on one stream, with CUDA events
+    between the stages: the whole span and each stage's duration, measured
+    live inside the timed region."""
+    import torch
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+          for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        for j, (_, c) in enumerate(calls):
+            c()
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    per = {name: [ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)]
+           for j, (name, _) in enumerate(calls)}
+    return {"ms": ev[0][0].elapsed_time(ev[-1][-1]),
+            "median": {k: statistics.median(v) for k, v in per.items()},
+            "mean": {k: statistics.fmean(v) for k, v in per.items()}}
+
+
+def product_rooflines(s: synth.LayerShape, mean_ms: dict, peak: float) -> dict:
+    """Tensor-pipe fractions of the two product stages (2 flop per
+    multiply-add of the gate/up and down products, all routed rows)."""
+    R = s.T * s.k
+    out = {}
+    for stage, flops in (("gate_up_swiglu", 2.0 * R * (2 * s.n_ff) * s.d),
+                         ("down", 2.0 * R * s.d * s.n_ff)):
+        ms = mean_ms[stage]
+        ach = flops / (ms * 1e-3) / 1e12 if ms > 0 else 0.0
+        out[stage] = {"launch_ms": ms, "achieved_tflops": ach, "frac": ach / peak}
+    return out
+
+
+def other_config_line(M, cfg: int, steps: int, warmup: int, dev: str, stream,
+                      peaks: dict, peak: float) -> dict:
+    """Configuration `cfg` timed in this process: the layer as its stage
+    sequence (as the main line), its binding roofline and the effective int8
+    rate."""
+    import torch
+    L = synth.config_layer(cfg)
+    s = L.shape
+    dl = DeviceLayer(M, L, dev)
+    calls = dl.stage_calls(stream)
+    for _ in range(warmup):
+        dl.layer(stream)
+    torch.cuda.synchronize()
+    if M.moe_read_status(dl.desc, dl.ws) != 0:
+        return {"workload": L.name, "error": "device status bits set"}
+    t = time_stages(calls, steps, stream)
+    ms = t["ms"] / steps
+    hbm = layer_bytes(L)
+    hbm_gbs = hbm["total"] / (ms * 1e-3) / 1e9
+    prod = product_rooflines(s, t["mean"], peak)
+    line = {"workload": L.name, "T": s.T, "steps": steps, "ms_per_step": ms,
+            "value": s.T / (ms * 1e-3), "unit": UNIT,
+            "effective_int8_tops": s.T / (ms * 1e-3) * s.k * ops_per_row(s) / 1e12,
+            "stage_ms": t["median"],
+            "roofline_tensor": {"kernel": "gate_up_swiglu", "peak": peak,
+                                "unit": "TFLOP/s", **prod["gate_up_swiglu"]},
+            "roofline_tensor_down": {"kernel": "down", "peak": peak, "unit": "TFLOP/s",
+                                     **prod["down"]},
+            "roofline_hbm": {"kernel": "layer", "achieved": hbm_gbs, "peak": peaks["hbm"],
+                             "unit": "GB/s", "frac": hbm_gbs / peaks["hbm"],
+                             "algorithmic_bytes": hbm["total"],
+                             "weights_bytes": hbm["weights"]},
+            "l2": l2_note(hbm)}
+    line["binding"] = ("hbm" if line["roofline_hbm"]["frac"] >
+                       line["roofline_tensor"]["frac"] else "tensor")
+    del dl
+    torch.cuda.empty_cache()
+    return line
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_setup(args)
@@ -308,24 +443,14 @@ def run_ours(args):
     L = config_layer(args)
     s = L.shape
     dev = f"cuda:{local}"
-    x = torch.from_numpy(L.x).to(dev)
-    ids = torch.from_numpy(L.topk_ids).to(dev)
-    w = torch.from_numpy(L.topk_w).to(dev)
-    # weights: uploaded row-major, tiled once (load time, outside every timed region)
-    desc, pack, eoff = M.tile_weights(s.T, s.d, s.n_ff, s.E, s.k, s.gu_fmt, s.down_fmt,
-                                      torch.from_numpy(L.weight_pack).to(dev),
-                                      torch.from_numpy(L.expert_offsets).to(dev),
-                                      gu_layout=s.gu_layout)
-    torch.cuda.synchronize()
-    out = torch.empty((s.T, s.d), dtype=torch.float32, device=dev)
-    ws = M.alloc_workspace(desc, dev)
     stream = torch.cuda.current_stream()
-
-    def layer():
-        M.moe_prefill_layer(desc, x, ids, w, pack, eoff, out, ws, stream)
+    dl = DeviceLayer(M, L, dev)
+    desc, x, ids, w, pack, eoff, out, ws = (dl.desc, dl.x, dl.ids, dl.w, dl.pack, dl.eoff,
+                                            dl.out, dl.ws)
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
 
     for _ in range(args.warmup):
-        layer()
+        dl.layer(stream)
     torch.cuda.synchronize()
     if M.moe_read_status(desc, ws) != 0:
         raise SystemExit("device status bits set")
@@ -334,39 +459,24 @@ def run_ours(args):
     # launch sequence (moe_prefill_layer's steps, one stage entry point each,
     # same stream), with CUDA events between the steps, so every kernel's
     # duration is measured live inside the timed region.
-    stages = ["route", "quant_q8", "gate_up_swiglu", "down", "combine"]
-    calls = [lambda: M.moe_route(desc, ids, ws, stream),
-             lambda: M.moe_quant_q8(desc, x, ws, stream),
-             lambda: M.moe_gate_up_swiglu(desc, pack, eoff, ws, stream),
-             lambda: M.moe_down(desc, pack, eoff, ws, stream),
-             lambda: M.moe_combine(desc, w, out, ws, stream)]
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
-          for _ in range(args.steps)]
+    calls = dl.stage_calls(stream)
     clocks = ClockSampler()
     if rank == 0:
         clocks.start()
     barrier(world)
     torch.cuda.synchronize()
     n0 = M.moe_kernel_launches()
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        for j, c in enumerate(calls):
-            c()
-            ev[i][j + 1].record(stream)
-    torch.cuda.synchronize()
+    t = time_stages(calls, args.steps, stream)
     launches = M.moe_kernel_launches() - n0
     barrier(world)
     clk = clocks.stop() if rank == 0 else None
-    ms = reduce_max(ev[0][0].elapsed_time(ev[-1][-1]), world)
+    ms = reduce_max(t["ms"], world)
     ms_per_step = ms / args.steps
     value = world * s.T * args.steps / (ms / 1e3)
-    stage_ms = {name: statistics.median(ev[i][j].elapsed_time(ev[i][j + 1])
-                                        for i in range(args.steps))
-                for j, name in enumerate(stages)}
-    gu_mean_ms = statistics.fmean(ev[i][2].elapsed_time(ev[i][3]) for i in range(args.steps))
+    stage_ms = t["median"]
     # the single-call entry point computes the same layer, bit for bit
     ref_out = out.clone()
-    layer()
+    dl.layer(stream)
     torch.cuda.synchronize()
     if not torch.equal(out, ref_out):
         raise SystemExit("moe_prefill_layer disagrees with its own stage sequence")
@@ -403,23 +513,27 @@ def run_ours(args):
     e2e_value = world * s.T * e2e_steps / (e2e_ms / 1e3)
     if not np.allclose(ho.numpy(), out.cpu().numpy(), rtol=0, atol=0):
         raise SystemExit("host-buffer entry point disagrees with the device entry point")
+    h2d = int(L.x.nbytes + L.topk_ids.nbytes + L.topk_w.nbytes)
+    del hx, hi, hw, ho, io
 
     if rank != 0:
         return 0
 
-    R = s.T * s.k
     peaks = load_peaks()
-    gu_ms = gu_mean_ms  # mean launch duration of gate/up inside the timed region
+    peak, peak_source = tensor_peak(peaks, clk)
+    prod = product_rooflines(s, t["mean"], peak)
+    gu = prod["gate_up_swiglu"]
+    R = s.T * s.k
     gu_flops = 2.0 * R * (2 * s.n_ff) * s.d
-    achieved = gu_flops / (gu_ms * 1e-3) / 1e12
     pairs = R * (2 * s.n_ff) * (s.d // 32)
-    sm_mhz = (clk or {}).get("sm_max_mhz") or 2070.0
-    alu_peak = SM_COUNT * FP32_LANES_PER_SM * sm_mhz * 1e6 / 1e12  # T lane-ops/s
-    alu_achieved = 2.0 * pairs / (gu_ms * 1e-3) / 1e12
+    sm_mhz = (clk or {}).get("sm_mhz") or (clk or {}).get("sm_max_mhz") or 2070.0
+    alu_peak = sm_count * FP32_LANES_PER_SM * sm_mhz * 1e6 / 1e12  # T lane-ops/s
+    alu_achieved = pairs / (gu["launch_ms"] * 1e-3) / 1e12
     eff_tops = value * s.k * ops_per_row(s) / 1e12
     # the recorded traffic and algorithmic bytes are for the configuration as listed
     variant = args.down_fmt is not None or args.gu_layout is not None
-    traffic = None if variant else measured_traffic(args.config)
+    traffic, traffic_source = ((None, "a format or layout variant of the configuration")
+                               if variant else measured_traffic(args.config))
     hbm = layer_bytes(L)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -436,20 +550,23 @@ def run_ours(args):
         "stage_ms": stage_ms,
         "roofline": {"bound": "tensor",
                      "kernel": "gate_up_swiglu (tcgen05 launch + small-row launch)",
-                     "achieved": achieved,
-                     "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["bf16_sustained"], "traffic": traffic,
-                     "peak_source": peaks["source"] + " bf16 dense, sustained (the kernel is "
-                                    "timed inside the layer's steps); fp16 operands run at "
-                                    "the bf16 rate",
+                     "achieved": gu["achieved_tflops"], "peak": peak, "unit": "TFLOP/s",
+                     "frac": gu["frac"], "traffic": traffic, "traffic_source": traffic_source,
+                     "peak_source": peak_source + "; fp16 operands run at the bf16 rate",
                      "algorithmic": f"2*R*2*n_ff*d = {gu_flops:.4g} flop per stage; "
                                     f"{ALGO_BYTES_GATE_UP.get(args.config, float('nan')):.4g} "
                                     "algorithmic bytes per stage",
-                     "launch_ms": gu_ms},
+                     "launch_ms": gu["launch_ms"]},
+        "roofline_down": {"bound": "tensor", "kernel": "down (tcgen05 + small-row launch)",
+                          "achieved": prod["down"]["achieved_tflops"], "peak": peak,
+                          "unit": "TFLOP/s", "frac": prod["down"]["frac"],
+                          "launch_ms": prod["down"]["launch_ms"]},
         "roofline_alu": {"bound": "alu", "kernel": "gate_up_swiglu", "achieved": alu_achieved,
-                         "peak": alu_peak, "unit": "T fp32 lane-ops/s",
+                         "peak": alu_peak, "unit": "T fp32 fma/s",
                          "frac": alu_achieved / alu_peak,
-                         "algorithmic": "2 ops (mul, fma) per (output, 32-value block)"},
+                         "algorithmic": "one fma per (output, 32-value block); "
+                                        f"{sm_count} SMs x {FP32_LANES_PER_SM} fp32 lanes x "
+                                        f"{sm_mhz:.0f} MHz"},
         "roofline_hbm": {"bound": "hbm", "kernel": "layer (all launches of a step)",
                          "achieved": hbm["total"] / (ms_per_step * 1e-3) / 1e9,
                          "peak": peaks["hbm"], "unit": "GB/s",
@@ -464,12 +581,20 @@ def run_ours(args):
                                   "tensor peak (mma.sync s8, measured); the products run as "
                                   "exact fp16 integers instead"},
         "graph": graph,
-        "e2e": {"value": e2e_value, "unit": UNIT,
-                "h2d_bytes_per_step": int(L.x.nbytes + L.topk_ids.nbytes + L.topk_w.nbytes),
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": int(s.T * s.d * 4)},
         "gpu_launches": int(launches),
         "clocks": clk,
     }
+    if world == 1 and not args.no_other_configs and not variant:
+        # the other benched layers of the spec, timed in this process (their
+        # own lines, not part of `value`); the main layer's buffers go first
+        del dl, x, ids, w, pack, eoff, out, ws, ref_out
+        torch.cuda.empty_cache()
+        line["other_configs"] = {
+            str(c): other_config_line(M, c, max(20, args.steps), args.warmup, dev, stream,
+                                      peaks, peak)
+            for c in OTHER_CONFIGS if c != args.config}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(L, args.cpu_tokens)
     print(json.dumps(line), flush=True)
@@ -490,6 +615,8 @@ def main_args(argv):
     ap.add_argument("--cpu-tokens", type=int, default=2048)
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the other configurations' lines")
     ap.add_argument("--down-fmt", choices=["w2", "w4nl", "q8_0"], default=None,
                     help="the configuration with its down matrices in another format")
     ap.add_argument("--gu-layout", choices=["split", "interleaved"], default=None,

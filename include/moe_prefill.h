@@ -288,11 +288,14 @@ int moe_read_status(const MoeLayerDesc *desc, void *workspace,
  * every GPU that loads the library until the process exits) instead of a
  * workspace: ceil(T*k/1024)*E + 4*floor(T*k/128) + 9*E + 71 int32 must fit
  * in 262144 (T*k = 163840 with E = 512 needs about 92,000), or
- * MOE_ERR_SCRATCH is returned with nothing enqueued.  The first call on a
- * device looks the array's device address up (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.  All
- * calls share the array: calls whose work overlaps on the GPU (other streams,
- * other threads) race.  Nothing is allocated or freed. */
+ * MOE_ERR_SCRATCH is returned with nothing enqueued.  Every call looks the
+ * array's device address up (cudaGetSymbolAddress) with the current device
+ * current; the first call on a device also loads the library's device code
+ * there, so make it before any stream capture.  No status word reaches the
+ * caller on this path: an expert id outside [0, E) shows only as dst_of = -1
+ * for that entry (and offsets[E] < T*k).  All calls share the array: calls
+ * whose work overlaps on the GPU (other streams, other threads) race.
+ * Nothing is allocated or freed. */
 int moe_route_noalloc(const MoeLayerDesc *desc, const int32_t *topk_ids,
                       int32_t *counts, int32_t *offsets, int32_t *row_src,
                       int32_t *dst_of, moe_stream_t stream);

@@ -1,5 +1,7 @@
 // C ABI of libmoeprefill.so: argument validation, workspace layout and the
 // order of the stages.  See include/moe_prefill.h for the contract.
+#include <cuda.h>
+
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -26,6 +28,36 @@ int device_sm_count() {
     return 1;
   if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
+}
+
+// The two driver calls are looked up through the runtime (as the tensor-map
+// encoder is), so that loading the library needs no libcuda on a host
+// without a GPU.
+uint64_t current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || !c ||
+      get_id(c, &id) != CUDA_SUCCESS)
+    return 0;
+  return (uint64_t)id;
 }
 
 namespace {
@@ -136,14 +168,15 @@ inline int launch_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR
 // forks from the caller's stream and joins back before the call returns, so
 // to the caller the stage is ordered on its own stream as before (also under
 // stream capture, where the fork and join become graph edges).  One stream
-// and two events per device, created on the first call that is not being
-// captured and kept until the process exits; calls enqueue under a lock, as
-// the events are shared.  Without them the two launches share the caller's
-// stream.
+// and two events per device and context, created on the first call that is
+// not being captured and kept until the process exits (a context replaced by
+// cudaDeviceReset gets new ones); calls enqueue under a lock, as the events
+// are shared.  Without them the two launches share the caller's stream.
 struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
-  bool tried = false;
+  uint64_t ctx = 0;    // context the handles belong to
+  bool tried = false;  // creation was attempted in that context
 };
 std::mutex g_side_mu;
 SideStream g_side[64];
@@ -152,11 +185,15 @@ SideStream* side_stream(cudaStream_t st) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   SideStream& sd = g_side[dev];
+  const uint64_t ctx = current_context_id();
+  if (ctx == 0) return nullptr;
+  if (sd.ctx != ctx) sd = SideStream{};  // handles of a destroyed context are dead
   if (!sd.s && !sd.tried) {
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
       return nullptr;
     sd.tried = true;
+    sd.ctx = ctx;
     if (cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking) != cudaSuccess ||
         cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess) {

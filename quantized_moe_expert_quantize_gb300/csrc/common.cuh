@@ -117,4 +117,9 @@ cudaError_t launch_tile_weights(const MoeLayerDesc& d, const uint8_t* src, int64
 
 int device_sm_count();
 
+// Identity of the current CUDA context (cuCtxGetId), 0 if there is none.
+// One-time set-up per device (kernel attributes, the side stream) is keyed
+// on it, so that it is redone in a new context after cudaDeviceReset.
+uint64_t current_context_id();
+
 }  // namespace moe

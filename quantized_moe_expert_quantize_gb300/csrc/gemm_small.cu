@@ -34,6 +34,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -568,15 +569,17 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_small() {
   return fn;
 }
 
-// Resident CTAs a multiprocessor (two by design), found once per device.
+// Resident CTAs a multiprocessor (two by design), found once per device and
+// context together with the kernel's attributes.
 template <int FMT, int MODE>
 cudaError_t launch_small(const SmArgs& a, const CUtensorMap& tm, const CUtensorMap& td,
                          int64_t items, cudaStream_t st) {
-  static int per_sm[64] = {0};
+  static std::atomic<uint64_t> ready[64];
+  static std::atomic<int> per_sm[64];
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!per_sm[dev]) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const uint64_t ctx = current_context_id();
+  if (ctx == 0 || ready[dev].load(std::memory_order_acquire) != ctx) {
     // two CTAs a multiprocessor: the full shared-memory carveout
     cudaError_t e = cudaFuncSetAttribute(
         gemm_small_kernel<FMT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -590,10 +593,13 @@ cudaError_t launch_small(const SmArgs& a, const CUtensorMap& tm, const CUtensorM
                                                          kSmemBytes);
     if (e != cudaSuccess) return e;
     if (n < 1) return cudaErrorInvalidConfiguration;
-    per_sm[dev] = n;
+    per_sm[dev].store(n, std::memory_order_relaxed);
+    ready[dev].store(ctx, std::memory_order_release);
   }
   const int grid =
-      (int)std::max<int64_t>(1, std::min<int64_t>(items, (int64_t)per_sm[dev] * device_sm_count()));
+      (int)std::max<int64_t>(
+          1, std::min<int64_t>(items, (int64_t)per_sm[dev].load(std::memory_order_relaxed) *
+                                          device_sm_count()));
   gemm_small_kernel<FMT, MODE><<<grid, kThreads, kSmemBytes, st>>>(a, tm, td);
   return cudaSuccess;
 }

@@ -60,6 +60,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -329,6 +330,17 @@ __device__ __forceinline__ void swiglu_q8_block_store(float2* acc, __half* hq, f
   st_global_v8_u32(hq, w);
   st_global_v8_u32(hq + 16, w + 8);
   *dh = d;
+}
+
+// Exit drain of a producer's ring: `issued` copies were armed on the full
+// barriers full[i % n] (phase parity (i / n) & 1); the consumers waited for
+// all but possibly the last n of them.  Waits for those with the polling
+// wait, bounded by its count alone (not cut short by the abort flag), so no
+// bulk or tensor copy is still writing shared memory when the CTA exits.
+__device__ __forceinline__ void drain_ring(uint64_t* full, uint32_t n, uint32_t issued,
+                                           volatile int* abort) {
+  for (uint32_t i = issued > n ? issued - n : 0; i < issued; i++)
+    if (!mbar_wait(&full[i % n], (i / n) & 1, abort, kTimeoutNs, false)) break;
 }
 
 // ---------------------------------------------------------------- kernel
@@ -644,6 +656,9 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
           tma_load_2d(sA + st * kABytes, &tmap, s * kSK, I.row0, &full_tma[st]);
         }
       }
+      // exit drain: copies the MMA never waited for (after an abort) land
+      // before the CTA exits; only the last kStages can still be in flight
+      drain_ring(full_tma, kStages, it, s_abort);
     }
     __syncwarp();
   } else if (warp == kWarpScales) {
@@ -667,6 +682,7 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
           tma_load_2d(sDx + de * (kTM * kScaleBox), &tmap_d, 4 * j, I.row0, &dfull[de]);
         }
       }
+      drain_ring(dfull, kDxRing, gd, s_abort);
     }
     __syncwarp();
   } else if (warp == kWarpRaw) {
@@ -692,6 +708,7 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
                    bytes, &rfull[slot]);
         }
       }
+      drain_ring(rfull, 2, issued, s_abort);
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
@@ -738,9 +755,12 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
           mma_commit(&empty[st]);
         }
       }
-      // drain: every MMA issued above has completed once this arrives
+      // drain: every MMA issued above has completed once this arrives (a
+      // polling wait, bounded by its count alone: it does not give up early
+      // when another role has set the abort flag, so TMEM is never freed
+      // under a running MMA)
       mma_commit(fin);
-      mbar_wait(fin, 0, s_abort, kTimeoutNs);
+      mbar_wait(fin, 0, s_abort, kTimeoutNs, false);
     }
     __syncwarp();
   }
@@ -774,17 +794,19 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 // would leave the epilogue's register increase waiting forever).
 template <int FMT, int MODE>
 cudaError_t prepare_kernel() {
-  static bool done[64] = {false};
+  // once per device and context (the attribute does not outlive the context)
+  static std::atomic<uint64_t> ready[64];
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const uint64_t ctx = current_context_id();
+  if (ctx != 0 && ready[dev].load(std::memory_order_acquire) == ctx) return cudaSuccess;
   cudaFuncAttributes attr;
   cudaError_t e = cudaFuncGetAttributes(&attr, gemm_tc_kernel<FMT, MODE>);
   if (e != cudaSuccess) return e;
   if (attr.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
   e = cudaFuncSetAttribute(gemm_tc_kernel<FMT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes);
-  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  if (e == cudaSuccess) ready[dev].store(ctx, std::memory_order_release);
   return e;
 }
 

@@ -20,7 +20,7 @@
 //                       time; __match_any_sync groups lanes of equal expert,
 //                       a lane's rank among them keeps flat order, so rows of
 //                       a bucket come out in increasing flat index t*k + r.
-#include <mutex>
+#include <atomic>
 
 #include "common.cuh"
 
@@ -302,15 +302,17 @@ cudaError_t launch_route(const int32_t* ids, int64_t n, int E, int32_t* hist,
   if (n <= kFusedMaxEntries) {
     // one launch; its per-warp counts take 32*E int32 of shared memory
     const size_t fsmem = sizeof(int32_t) * kFusedWarps * E;
-    static bool ready[64] = {false};
+    // the shared-memory attribute is set once per device and context
+    static std::atomic<uint64_t> ready[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!ready[dev]) {
+    const uint64_t ctx = current_context_id();
+    if (ctx == 0 || ready[dev].load(std::memory_order_acquire) != ctx) {
       const cudaError_t e = cudaFuncSetAttribute(
           route_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
           (int)(sizeof(int32_t) * kFusedWarps * 1024));
       if (e != cudaSuccess) return e;
-      ready[dev] = true;
+      ready[dev].store(ctx, std::memory_order_release);
     }
     route_fused_kernel<<<1, 1024, fsmem, st>>>(ids, n, E, counts, offsets, order, tiles, ntiles,
                                                row_src, dst_of, status);
@@ -351,8 +353,8 @@ namespace {
 constexpr int64_t kNoAllocScratchInts = 1 << 18;  // 1 MiB of int32
 static __device__ __align__(256) int32_t g_route_scratch[kNoAllocScratchInts];
 
-// layout in ints: [0] status bits, [1] tile count, [64..] expert order,
-// then the tile list (int4), then the chunk histogram
+// layout in ints: [0] status bits, [1..2] the tile counts, [64..] expert
+// order, then the tile list (int4), then the chunk histogram
 struct NoAllocLayout {
   int64_t order, tiles, hist, total;
 };
@@ -365,27 +367,19 @@ NoAllocLayout noalloc_layout(int64_t n, int E) {
   return L;
 }
 
-// Device address of the scratch array on the current device, found once per
-// device with that device current.  The host-side name of the array is only
-// a stand-in and must never be handed to a kernel.
+// Device address of the scratch array in the current device's context,
+// looked up on every call with that device current (a lookup is cheap, and
+// an address kept from an earlier context would dangle after
+// cudaDeviceReset).  The host-side name of the array is only a stand-in and
+// must never be handed to a kernel.
 int32_t* noalloc_scratch(int* err) {
-  static std::mutex mu;
-  static int32_t* addr[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-    *err = MOE_ERR_DEVICE;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) {
+    cudaGetLastError();
+    *err = MOE_ERR_LAUNCH;
     return nullptr;
   }
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) {
-      *err = MOE_ERR_LAUNCH;
-      return nullptr;
-    }
-    addr[dev] = static_cast<int32_t*>(p);
-  }
-  return addr[dev];
+  return static_cast<int32_t*>(p);
 }
 
 }  // namespace
