@@ -161,6 +161,38 @@ def graph_leg(M, layer_call, out, ref_out, steps: int, world: int, T: int) -> di
         return {"error": f"{type(exc).__name__}: {exc}"[:200]}
 
 
+def fused_combine_leg(M, dl, ref_out, steps: int, world: int, stream) -> dict:
+    """ms per layer step of the single-call layer, unfused and with the
+    combine fused into the down epilogue, timed back to back."""
+    import copy
+    import torch
+    try:
+        fd = copy.copy(dl.desc)
+        fd.flags = M.MOE_FLAG_FUSED_COMBINE
+        out = torch.empty_like(dl.out)
+
+        def run(desc, n):
+            for _ in range(n):
+                M.moe_prefill_layer(desc, dl.x, dl.ids, dl.w, dl.pack, dl.eoff, out, dl.ws, stream)
+
+        res = {}
+        for name, desc in (("unfused", dl.desc), ("fused", fd)):
+            run(desc, 2)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run(desc, steps)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            res[name + "_ms_per_step"] = reduce_max(e0.elapsed_time(e1), world) / steps
+            if not torch.equal(out, ref_out):
+                return {"error": f"{name} layer disagrees with the stage sequence"}
+        return res
+    except Exception as exc:  # reported, not fatal
+        return {"error": f"{type(exc).__name__}: {exc}"[:200]}
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -481,6 +513,11 @@ def run_ours(args):
     if not torch.equal(out, ref_out):
         raise SystemExit("moe_prefill_layer disagrees with its own stage sequence")
 
+    # ---- A/B of the combine fused into the down epilogue: the single-call
+    # layer with and without MOE_FLAG_FUSED_COMBINE, back to back (the
+    # fused layer must give the same bits)
+    fused = fused_combine_leg(M, dl, ref_out, args.steps, world, stream)
+
     # ---- the single-call layer captured once in a CUDA graph and replayed:
     # the same kernels without the host's launch gaps (reported beside
     # `value`, which times the launch sequence itself)
@@ -581,6 +618,7 @@ def run_ours(args):
                                   "tensor peak (mma.sync s8, measured); the products run as "
                                   "exact fp16 integers instead"},
         "graph": graph,
+        "fused_combine": fused,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": int(s.T * s.d * 4)},
         "gpu_launches": int(launches),

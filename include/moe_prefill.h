@@ -78,6 +78,19 @@ enum { MOE_FMT_W2 = 1, MOE_FMT_W4NL = 2, MOE_FMT_Q8_0 = 3 };
  * H = silu(gate)*up pairs gate j with up j either way. */
 enum { MOE_GU_SPLIT = 0, MOE_GU_INTERLEAVED = 1 };
 
+/* Layer flags (MoeLayerDesc.flags).
+ *   MOE_FLAG_FUSED_COMBINE  moe_prefill_layer runs the combine inside the
+ *     down product's epilogue instead of as a pass of its own: after a
+ *     routed row's Dm values of a 32-column group are stored, the row counts
+ *     itself in for its token and group (a device-scope atomic after a
+ *     fence); the last of the token's k rows to arrive sums the k rows of
+ *     the group in rank order, one fma per rank -- the same arithmetic as
+ *     moe_combine, so out is bit-identical either way ("Strata #3752",
+ *     Validation: the prompt path's combine fused with the write).  Dm is
+ *     still written (a row cannot know it is the last before it has
+ *     published its values). */
+enum { MOE_FLAG_FUSED_COMBINE = 1 };
+
 enum {
   MOE_OK = 0,
   MOE_ERR_NULL = -1,        /* a required pointer is NULL                  */
@@ -112,7 +125,7 @@ typedef struct MoeLayerDesc {
   int32_t gu_fmt;   /* MOE_FMT_* of the gate/up matrices              */
   int32_t down_fmt; /* MOE_FMT_* of the down matrices                 */
   int32_t gu_layout;/* MOE_GU_SPLIT or MOE_GU_INTERLEAVED            */
-  uint32_t flags;   /* must be 0                                      */
+  uint32_t flags;   /* MOE_FLAG_* bits (0 = none)                     */
   int32_t reserved; /* must be 0                                      */
   int64_t weight_pack_bytes; /* size of the tiled weight pack; expert matrices must lie inside */
 } MoeLayerDesc;
@@ -263,6 +276,14 @@ int moe_swiglu_quant(const MoeLayerDesc *desc, void *workspace,
 int moe_down(const MoeLayerDesc *desc, const uint8_t *weight_pack,
              const int64_t *expert_offsets, void *workspace,
              size_t workspace_bytes, moe_stream_t stream);
+/* The down product with the combine fused into its epilogue (the step
+ * moe_prefill_layer runs under MOE_FLAG_FUSED_COMBINE; here regardless of
+ * the flag): writes dm and out [T x d] (device fp32, 16-byte aligned) from
+ * topk_w (device fp32 [T x k]), the routing of moe_route and the workspace's
+ * hq and dh. */
+int moe_down_combine(const MoeLayerDesc *desc, const uint8_t *weight_pack,
+                     const int64_t *expert_offsets, const float *topk_w, float *out,
+                     void *workspace, size_t workspace_bytes, moe_stream_t stream);
 int moe_combine(const MoeLayerDesc *desc, const float *topk_w, float *out,
                 void *workspace, size_t workspace_bytes, moe_stream_t stream);
 

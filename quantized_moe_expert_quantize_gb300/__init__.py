@@ -21,6 +21,7 @@ MOE_FMT_W4NL = 2
 MOE_FMT_Q8_0 = 3
 MOE_GU_SPLIT = 0
 MOE_GU_INTERLEAVED = 1
+MOE_FLAG_FUSED_COMBINE = 1
 
 MOE_OK = 0
 MOE_ERR_NULL = -1
@@ -42,7 +43,8 @@ MOE_STATUS_BAD_ROUTING = 8
 EXPORTS = (
     "moe_prefill_workspace_bytes", "moe_workspace_view", "moe_prefill_layer",
     "moe_host_io_bytes", "moe_prefill_layer_host", "moe_route", "moe_quant_q8",
-    "moe_gate_up", "moe_swiglu_quant", "moe_down", "moe_combine", "moe_read_status",
+    "moe_gate_up", "moe_swiglu_quant", "moe_down", "moe_down_combine", "moe_combine",
+    "moe_read_status",
     "moe_check_device", "moe_status_string", "moe_kernel_launches", "moe_route_noalloc",
     "moe_tiled_pack_bytes", "moe_tile_weights", "moe_gate_up_swiglu",
     "moe_selftest_wait_timeout",
@@ -109,6 +111,8 @@ def lib(build_if_missing: bool = False) -> ctypes.CDLL:
         L.moe_swiglu_quant.restype = i32
         L.moe_down.argtypes = [dp, vp, vp, vp, sz, vp]
         L.moe_down.restype = i32
+        L.moe_down_combine.argtypes = [dp, vp, vp, vp, vp, vp, sz, vp]
+        L.moe_down_combine.restype = i32
         L.moe_combine.argtypes = [dp, vp, vp, vp, sz, vp]
         L.moe_combine.restype = i32
         L.moe_route_noalloc.argtypes = [dp, vp, vp, vp, vp, vp, vp]
@@ -141,8 +145,8 @@ def _check(rc: int, where: str):
 
 
 def make_desc(T, d, n_ff, E, k, gu_fmt=MOE_FMT_W2, down_fmt=MOE_FMT_W2,
-              weight_pack_bytes=0, gu_layout=MOE_GU_SPLIT) -> MoeLayerDesc:
-    return MoeLayerDesc(T, d, n_ff, E, k, gu_fmt, down_fmt, int(gu_layout), 0, 0,
+              weight_pack_bytes=0, gu_layout=MOE_GU_SPLIT, flags=0) -> MoeLayerDesc:
+    return MoeLayerDesc(T, d, n_ff, E, k, gu_fmt, down_fmt, int(gu_layout), int(flags), 0,
                         int(weight_pack_bytes))
 
 
@@ -301,6 +305,13 @@ def moe_down(desc, weight_pack, expert_offsets, workspace, stream=None):
     _check(lib().moe_down(ctypes.byref(desc), _ptr(weight_pack, torch.uint8),
                           _ptr(expert_offsets, torch.int64), _ptr(workspace, torch.uint8),
                           workspace.numel(), _stream(stream)), "moe_down")
+
+
+def moe_down_combine(desc, weight_pack, expert_offsets, topk_w, out, workspace, stream=None):
+    _check(lib().moe_down_combine(ctypes.byref(desc), _ptr(weight_pack, torch.uint8),
+                                  _ptr(expert_offsets, torch.int64), _ptr(topk_w, torch.float32),
+                                  _ptr(out, torch.float32), _ptr(workspace, torch.uint8),
+                                  workspace.numel(), _stream(stream)), "moe_down_combine")
 
 
 def moe_combine(desc, topk_w, out, workspace, stream=None):

@@ -66,7 +66,7 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t status, counts, offsets, order, tiles, row_src, dst_of, hist, xq, dx, gu, hq, dh, dm;
+  size_t status, counts, offsets, order, tiles, row_src, dst_of, hist, xq, dx, gu, hq, dh, dm, cnt;
   size_t total;
 };
 
@@ -96,6 +96,7 @@ Layout layout(const MoeLayerDesc& d) {
   L.hq = take(sizeof(uint16_t) * (size_t)R * d.n_ff);
   L.dh = take(sizeof(float) * (size_t)R * scale_stride(d.n_ff));
   L.dm = take(sizeof(float) * (size_t)R * d.d);
+  L.cnt = take(sizeof(int32_t) * (size_t)d.T * (d.d / 32));  // fused combine's counters
   L.total = p;
   return L;
 }
@@ -109,7 +110,8 @@ int validate_desc(const MoeLayerDesc* d) {
   if ((int64_t)d->T * d->k >= ((int64_t)1 << 24)) return MOE_ERR_SHAPE;
   auto fmt_ok = [](int f) { return f == MOE_FMT_W2 || f == MOE_FMT_W4NL || f == MOE_FMT_Q8_0; };
   if (!fmt_ok(d->gu_fmt) || !fmt_ok(d->down_fmt) ||
-      (d->gu_layout != MOE_GU_SPLIT && d->gu_layout != MOE_GU_INTERLEAVED) || d->flags != 0 ||
+      (d->gu_layout != MOE_GU_SPLIT && d->gu_layout != MOE_GU_INTERLEAVED) ||
+      (d->flags & ~(uint32_t)MOE_FLAG_FUSED_COMBINE) != 0 ||
       d->reserved != 0)
     return MOE_ERR_FORMAT;
   if (d->weight_pack_bytes < 0) return MOE_ERR_SHAPE;
@@ -219,7 +221,7 @@ int run_quant(Ctx& c, const float* x, cudaStream_t st) {
 }
 
 int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaStream_t st,
-             bool fuse_swiglu = false) {
+             bool fuse_swiglu = false, const float* comb_w = nullptr, float* comb_out = nullptr) {
   GemmArgs a{};
   a.pack = pack;
   a.eoff = eoff;
@@ -248,6 +250,14 @@ int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaSt
     a.K = c.d.n_ff;
     a.N_out = c.d.d;
     a.out = c.v.dm;
+    if (comb_out) {
+      a.comb.out = comb_out;
+      a.comb.topk_w = comb_w;
+      a.comb.dst_of = c.v.dst_of;
+      a.comb.row_src = c.v.row_src;
+      a.comb.cnt = (int32_t*)(c.ws + c.L.cnt);
+      a.comb.k = c.d.k;
+    }
   }
   // 128-row tiles on the tcgen05 kernel, short remainders on the small-row
   // tier (both read the tile list's split point on the device), the latter
@@ -274,6 +284,25 @@ int run_swiglu(Ctx& c, cudaStream_t st) {
 
 int run_combine(Ctx& c, const float* w, float* out, cudaStream_t st) {
   return launch_rc(launch_combine(w, c.v.dst_of, c.v.dm, c.d.T, c.d.k, c.d.d, out, st));
+}
+
+// The down product with the combine fused into its epilogue: the arrival
+// counters first (on the caller's stream, before the products fork).
+int run_down_combine(Ctx& c, const uint8_t* pack, const int64_t* eoff, const float* w,
+                     float* out, cudaStream_t st) {
+  int rc = launch_rc(launch_combine_init(c.v.dst_of, c.d.T, c.d.k, c.d.d / 32,
+                                         (int32_t*)(c.ws + c.L.cnt), st));
+  if (rc) return rc;
+  return run_gemm(c, 1, pack, eoff, st, false, w, out);
+}
+
+// The layer's last two steps: down then combine, or both fused.
+int run_down_and_combine(Ctx& c, const uint8_t* pack, const int64_t* eoff, const float* w,
+                         float* out, cudaStream_t st) {
+  if (c.d.flags & MOE_FLAG_FUSED_COMBINE) return run_down_combine(c, pack, eoff, w, out, st);
+  int rc = run_gemm(c, 1, pack, eoff, st);
+  if (rc) return rc;
+  return run_combine(c, w, out, st);
 }
 
 int check_weights(const MoeLayerDesc* d, const uint8_t* pack, const int64_t* eoff) {
@@ -388,6 +417,19 @@ int moe_down(const MoeLayerDesc* desc, const uint8_t* pack, const int64_t* eoff,
   return run_gemm(c, 1, pack, eoff, (cudaStream_t)stream);
 }
 
+int moe_down_combine(const MoeLayerDesc* desc, const uint8_t* pack, const int64_t* eoff,
+                     const float* topk_w, float* out, void* ws, size_t bytes,
+                     moe_stream_t stream) {
+  Ctx c;
+  int rc = open_ctx(desc, ws, bytes, c);
+  if (rc) return rc;
+  if ((rc = check_weights(desc, pack, eoff))) return rc;
+  if ((!topk_w || !out) && c.d.T > 0) return MOE_ERR_NULL;
+  if (!aligned(out, 16)) return MOE_ERR_ALIGN;
+  if ((rc = check_device())) return rc;
+  return run_down_combine(c, pack, eoff, topk_w, out, (cudaStream_t)stream);
+}
+
 int moe_combine(const MoeLayerDesc* desc, const float* topk_w, float* out, void* ws, size_t bytes,
                 moe_stream_t stream) {
   Ctx c;
@@ -415,8 +457,7 @@ int moe_prefill_layer(const MoeLayerDesc* desc, const float* x, const int32_t* t
   if ((rc = run_route(c, topk_ids, st))) return rc;
   if ((rc = run_quant(c, x, st))) return rc;
   if ((rc = run_gemm(c, 0, weight_pack, expert_offsets, st, true))) return rc;
-  if ((rc = run_gemm(c, 1, weight_pack, expert_offsets, st))) return rc;
-  return run_combine(c, topk_w, out, st);
+  return run_down_and_combine(c, weight_pack, expert_offsets, topk_w, out, st);
 }
 
 size_t moe_host_io_bytes(const MoeLayerDesc* desc) {
@@ -457,8 +498,7 @@ int moe_prefill_layer_host(const MoeLayerDesc* desc, const float* h_x, const int
   if ((rc = run_route(c, d_ids, st))) return rc;
   if ((rc = run_quant(c, d_x, st))) return rc;
   if ((rc = run_gemm(c, 0, weight_pack, expert_offsets, st, true))) return rc;
-  if ((rc = run_gemm(c, 1, weight_pack, expert_offsets, st))) return rc;
-  if ((rc = run_combine(c, d_w, d_out, st))) return rc;
+  if ((rc = run_down_and_combine(c, weight_pack, expert_offsets, d_w, d_out, st))) return rc;
   if (T > 0 && cudaMemcpyAsync(h_out, d_out, bx, cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return MOE_ERR_LAUNCH;
   return MOE_OK;

@@ -81,6 +81,18 @@ cudaError_t launch_combine(const float* topk_w, const int32_t* dst_of, const flo
                            int64_t T, int k, int d, float* out, cudaStream_t st);
 
 // ------------------------------------------------------------ products
+// The combine fused into the down product's epilogue (when out is set): the
+// last of a token's rows to finish a 32-column group of Dm sums the token's
+// k rows in rank order into out [T x N_out].
+struct CombineArgs {
+  float* out;
+  const float* topk_w;       // [T x k]
+  const int32_t* dst_of;     // [T*k] flat entry -> routed row (-1: dropped)
+  const int32_t* row_src;    // [rows] routed row -> flat entry
+  int32_t* cnt;              // [T x N_out/32] arrivals per (token, group)
+  int k;
+};
+
 struct GemmArgs {
   const uint8_t* pack;       // device-tiled weight pack
   const int64_t* eoff;       // [E][2] byte offsets in the tiled pack
@@ -101,7 +113,60 @@ struct GemmArgs {
   float* dh;                 //   are written instead of GU
   int64_t rows_max;          // capacity of the routed-row buffers (T*k)
   int32_t* status;
+  CombineArgs comb;          // down only: the combine fused into the epilogue
 };
+
+// The fused combine's per-(token, 32-column group) arrival counters start
+// at the token's count of dropped ranks, so that the last of its valid rows
+// is the one that sees k - 1.
+cudaError_t launch_combine_init(const int32_t* dst_of, int64_t T, int k, int groups,
+                                int32_t* cnt, cudaStream_t st);
+
+// Sum of a token's k rows of Dm over one 32-column group in rank order (one
+// fma per rank, from 0), into out: the combine's arithmetic, run by the last
+// row to arrive.  Dm is read through L2 (other SMs wrote it).
+__device__ __forceinline__ void combine_group32(const float* __restrict__ dm, int64_t rows_max,
+                                                int N_out, const float* __restrict__ topk_w,
+                                                const int32_t* __restrict__ dst_of, int64_t t, int k,
+                                                int col0, float* __restrict__ out) {
+  float4 acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; j++) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int r = 0; r < k; r++) {
+    const int32_t pos = __ldcg(dst_of + t * k + r);
+    if (pos < 0 || pos >= rows_max) continue;  // dropped row
+    const float w = __ldcg(topk_w + t * k + r);
+    const float4* src = reinterpret_cast<const float4*>(dm + (int64_t)pos * N_out + col0);
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      const float4 v = __ldcg(src + j);
+      acc[j].x = fmaf(w, v.x, acc[j].x);
+      acc[j].y = fmaf(w, v.y, acc[j].y);
+      acc[j].z = fmaf(w, v.z, acc[j].z);
+      acc[j].w = fmaf(w, v.w, acc[j].w);
+    }
+  }
+  float4* dst = reinterpret_cast<float4*>(out + t * N_out + col0);
+#pragma unroll
+  for (int j = 0; j < 8; j++) dst[j] = acc[j];
+}
+
+// A routed row's arrival for its token's 32-column group starting at col0
+// of Dm [rows_max x N_out], after its values of the group are stored (by
+// this thread, or by its warp before a __syncwarp): fence, count in, and
+// combine the group if it is the last of the token's rows.
+__device__ __forceinline__ void combine_arrive(const CombineArgs& c, const float* dm,
+                                               int64_t rows_max, int N_out, int64_t row, int col0) {
+  const int32_t src = __ldcg(c.row_src + row);
+  if (src < 0 || src >= rows_max) return;
+  const int64_t t = src / c.k;
+  __threadfence();
+  const int old = atomicAdd(c.cnt + t * (N_out / 32) + col0 / 32, 1);
+  if (old == c.k - 1) {
+    __threadfence();
+    combine_group32(dm, rows_max, N_out, c.topk_w, c.dst_of, t, c.k, col0, c.out);
+  }
+}
 bool tc_supported(const MoeLayerDesc& d);
 // tcgen05 kernel: the tiles [0, ntiles[1])
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st);

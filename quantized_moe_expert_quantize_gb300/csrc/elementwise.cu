@@ -172,6 +172,19 @@ combine_kernel(const float* __restrict__ topk_w, const int32_t* __restrict__ dst
   out[g] = acc;
 }
 
+// Arrival counters of the fused combine: cnt[t][g] = the count of token t's
+// dropped ranks (dst_of < 0), for every 32-column group g.
+__global__ void __launch_bounds__(256)
+combine_init_kernel(const int32_t* __restrict__ dst_of, int64_t T, int k, int groups,
+                    int32_t* __restrict__ cnt) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= T * groups) return;
+  const int64_t t = i / groups;
+  int dropped = 0;
+  for (int r = 0; r < k; r++) dropped += dst_of[t * k + r] < 0;
+  cnt[i] = dropped;
+}
+
 inline unsigned blocks_for(int64_t threads, int per_block) {
   return (unsigned)((threads + per_block - 1) / per_block);
 }
@@ -194,6 +207,15 @@ cudaError_t launch_swiglu_quant(const float* gu, const int32_t* nrows_dev, int64
   if (groups == 0) return cudaSuccess;
   swiglu_quant_kernel<<<blocks_for(groups, 256), 256, 0, st>>>(gu, nrows_dev, rows_max, n_ff,
                                                                 gu_layout, hq, dh);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_init(const int32_t* dst_of, int64_t T, int k, int groups,
+                                int32_t* cnt, cudaStream_t st) {
+  const int64_t n = T * groups;
+  if (n == 0) return cudaSuccess;
+  combine_init_kernel<<<blocks_for(n, 256), 256, 0, st>>>(dst_of, T, k, groups, cnt);
   count_launch();
   return cudaGetLastError();
 }

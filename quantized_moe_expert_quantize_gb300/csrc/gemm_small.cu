@@ -98,6 +98,7 @@ struct SmArgs {
   float* dh;
   int64_t rows_max;
   int32_t* status;
+  CombineArgs comb;  // down: the combine fused into the epilogue (comb.out set)
 };
 
 __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
@@ -468,6 +469,13 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
             }
           }
         }
+        if (a.comb.out) {
+          // the warp stored the 32-column group 32w .. 32w+31 of every routed
+          // row of the tile; one lane per row counts it in
+          __syncwarp();
+          if (lane < u)
+            combine_arrive(a.comb, a.out, a.rows_max, a.N_out, (int64_t)t.y + lane, wt * kTN + 32 * warp);
+        }
       } else if (MODE == kModeGU) {
         if (!active) continue;
         const int n_ff = a.N_out >> 1;
@@ -626,6 +634,7 @@ cudaError_t launch_gemm_small(const GemmArgs& g, cudaStream_t st) {
   a.dh = g.dh;
   a.rows_max = g.rows_max;
   a.status = g.status;
+  a.comb = g.comb;
 
   auto encode = get_encode_small();
   if (!encode) return cudaErrorNotSupported;

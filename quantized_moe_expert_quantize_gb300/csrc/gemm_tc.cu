@@ -149,6 +149,7 @@ struct TcArgs {
   float* dh;            // fused swiglu_quant: scales [rows x scale_stride(N_out/2)]
   int64_t rows_max;
   int32_t* status;
+  CombineArgs comb;     // down: the combine fused into the epilogue (comb.out set)
 };
 
 struct Item {
@@ -530,6 +531,11 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
         float* outp = a.out + row * a.N_out + I.o0 + 64 * h;
 #pragma unroll
         for (int j = 0; j < 8; j++) st_global_v8(outp + 8 * j, acc + 4 * j);
+        if (a.comb.out) {
+          // this thread stored both 32-column groups of its row
+          combine_arrive(a.comb, a.out, a.rows_max, a.N_out, row, I.o0 + 64 * h);
+          combine_arrive(a.comb, a.out, a.rows_max, a.N_out, row, I.o0 + 64 * h + 32);
+        }
       } else if (MODE == kModeGU) {
         // gate outputs 128t + 32h .. + 31, and the matching up outputs
         const int o = (I.o0 >> 1) + 32 * h;
@@ -837,6 +843,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
   a.gu_layout = g.gu_layout;
   a.rows_max = g.rows_max;
   a.status = g.status;
+  a.comb = g.comb;
 
   auto encode = get_encode();
   if (!encode) return cudaErrorNotSupported;

@@ -55,7 +55,7 @@ def test_workspace_bytes_layout(lib):
     ("E", 0, M.MOE_ERR_SHAPE), ("E", 2048, M.MOE_ERR_SHAPE), ("k", 0, M.MOE_ERR_SHAPE),
     ("k", 9, M.MOE_ERR_SHAPE), ("T", -1, M.MOE_ERR_SHAPE), ("gu_fmt", 4, M.MOE_ERR_FORMAT),
     ("down_fmt", 0, M.MOE_ERR_FORMAT), ("gu_layout", 2, M.MOE_ERR_FORMAT),
-    ("flags", 1, M.MOE_ERR_FORMAT)])
+    ("flags", 2, M.MOE_ERR_FORMAT), ("flags", 3, M.MOE_ERR_FORMAT)])
 def test_bad_descriptor_rejected(lib, field, value, code):
     d = M.make_desc(64, 256, 64, 8, 2)
     setattr(d, field, value)
@@ -64,6 +64,14 @@ def test_bad_descriptor_rejected(lib, field, value, code):
     rc = lib.moe_prefill_layer(ctypes.byref(d), 16, 16, 16, 16, 16, 16, ctypes.addressof(ws),
                                1 << 20, None)
     assert rc == code
+
+
+def test_fused_combine_flag_is_accepted(lib):
+    """MOE_FLAG_FUSED_COMBINE is the one known flag: the layer keeps its
+    workspace size (the fused combine's counters are always laid out)."""
+    d0 = M.make_desc(64, 256, 64, 8, 2)
+    d1 = M.make_desc(64, 256, 64, 8, 2, flags=M.MOE_FLAG_FUSED_COMBINE)
+    assert M.workspace_bytes(d1) == M.workspace_bytes(d0) > 0
 
 
 def _fake(addr):

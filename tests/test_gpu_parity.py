@@ -126,6 +126,53 @@ def test_fused_swiglu_equals_stages(M, name):
     assert np.array_equal(dl.get("dh", R), dh_f)
 
 
+@pytest.mark.parametrize("name", ["cfg0_tiny", "mid_w2_w2", "mid_w2_w4nl", "mid_w2_q8",
+                                  "flat_w4nl_q8"])
+def test_fused_combine_equals_unfused(M, name):
+    """The combine fused into the down epilogue (MOE_FLAG_FUSED_COMBINE)
+    gives the unfused layer's out bit for bit: the last of a token's rows
+    to finish a 32-column group sums the k rows in rank order, one fma per
+    rank, as the combine step does; the stage entry point moe_down_combine
+    does the same after the earlier stages."""
+    L = SMALL[name]()
+    s = L.shape
+    a = DeviceLayer(M, L)
+    a.run_layer()
+    assert a.status() == 0
+    ref = a.out.clone()
+    b = DeviceLayer(M, L)
+    b.desc.flags = M.MOE_FLAG_FUSED_COMBINE
+    b.run_layer()
+    assert b.status() == 0
+    assert torch.equal(b.out, ref)
+    R = int(a.get("offsets")[-1])
+    assert np.array_equal(b.get("dm", R), a.get("dm", R))
+    # the stage entry point, on a fresh output, twice in a row (the arrival
+    # counters are set again by every call)
+    for _ in range(2):
+        b.out.fill_(float("nan"))
+        M.moe_down_combine(b.desc, b.pack, b.eoff, b.w, b.out, b.ws)
+        torch.cuda.synchronize()
+        assert torch.equal(b.out, ref)
+
+
+def test_fused_combine_with_dropped_rows(M):
+    """A token whose rank has an out-of-range expert id has one routed row
+    fewer; its groups complete at k - 1 arrivals and out still matches the
+    unfused layer bit for bit."""
+    shape = synth.LayerShape(40, 256, 64, 8, 2)
+    L = synth.make_layer(shape, seed=5, routing="topk")
+    L.topk_ids[4, 1] = 8
+    L.topk_ids[11, 0] = -3
+    a = DeviceLayer(M, L)
+    a.run_layer()
+    b = DeviceLayer(M, L)
+    b.desc.flags = M.MOE_FLAG_FUSED_COMBINE
+    b.run_layer()
+    assert b.status() & M.MOE_STATUS_BAD_EXPERT_ID
+    assert torch.equal(b.out, a.out)
+
+
 def test_config4_full_parity(M):
     """T=128 full layer (the weight-bandwidth-bound configuration), every
     output against the full oracle."""
@@ -432,6 +479,12 @@ def test_tile_split_row_counts(M, fmts):
         assert dl.status() == 0
         assert dl.get("counts").tolist() == SPLIT_COUNTS
         check_full(dl, o)
+    # the combine fused into the down epilogue, on both product kernels
+    ref = dl.out.clone()
+    dl.desc.flags = M.MOE_FLAG_FUSED_COMBINE
+    dl.run_layer()
+    assert dl.status() == 0
+    assert torch.equal(dl.out, ref)
 
 
 def _two_expert_ids(T: int) -> np.ndarray:
