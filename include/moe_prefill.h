@@ -238,10 +238,17 @@ int moe_prefill_layer(const MoeLayerDesc *desc, const float *x,
  * memory makes the copies asynchronous; pageable memory works but the copies
  * then synchronise).  The weights, offsets and workspace stay on the device.
  * The host inputs are copied into `io`, a caller-owned device staging buffer
- * of moe_host_io_bytes(desc) bytes (256-byte aligned), with one
- * cudaMemcpyAsync per array; out is copied back the same way.  The call
- * returns after enqueueing: the caller synchronises `stream` before reading
- * out or reusing the host inputs. */
+ * of moe_host_io_bytes(desc) bytes (256-byte aligned); out is copied back
+ * from it.  The call returns after enqueueing: the caller synchronises
+ * `stream` before reading out or reusing the host inputs.
+ * The transfers overlap compute where the order allows: x is copied on a
+ * per-device copy stream that waits only until the previous call on the same
+ * `io` has quantised its x (so a call enqueued while the previous one
+ * computes brings its x in meanwhile), and out leaves in token chunks on a
+ * second copy stream right behind the combine; `stream` waits for the last
+ * chunk.  Calls whose work overlaps on the same `io` (other streams, other
+ * threads) race, as on one workspace.  Under stream capture all copies run
+ * on `stream` in order. */
 size_t moe_host_io_bytes(const MoeLayerDesc *desc);
 int moe_prefill_layer_host(const MoeLayerDesc *desc, const float *h_x,
                            const int32_t *h_topk_ids, const float *h_topk_w,

@@ -177,6 +177,11 @@ inline int launch_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR
 struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
+  // moe_prefill_layer_host's copy streams and their events (see there)
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t x_in = nullptr, x_free = nullptr, comb = nullptr, out_done = nullptr,
+              entry = nullptr;
+  const void* last_io = nullptr;  // staging buffer x_free was last recorded for
   uint64_t ctx = 0;    // context the handles belong to
   bool tried = false;  // creation was attempted in that context
 };
@@ -198,7 +203,14 @@ SideStream* side_stream(cudaStream_t st) {
     sd.ctx = ctx;
     if (cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking) != cudaSuccess ||
         cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess) {
+        cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&sd.h2d, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&sd.d2h, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&sd.x_in, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&sd.x_free, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&sd.comb, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&sd.out_done, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&sd.entry, cudaEventDisableTiming) != cudaSuccess) {
       cudaGetLastError();
       sd.s = nullptr;
       return nullptr;
@@ -283,7 +295,8 @@ int run_swiglu(Ctx& c, cudaStream_t st) {
 }
 
 int run_combine(Ctx& c, const float* w, float* out, cudaStream_t st) {
-  return launch_rc(launch_combine(w, c.v.dst_of, c.v.dm, c.d.T, c.d.k, c.d.d, out, st));
+  return launch_rc(
+      launch_combine(w, c.v.dst_of, c.v.dm, 0, c.d.T, c.d.k, c.d.d, rows_max(c.d), out, st));
 }
 
 // The down product with the combine fused into its epilogue: the arrival
@@ -467,6 +480,23 @@ size_t moe_host_io_bytes(const MoeLayerDesc* desc) {
          align_up(sizeof(float) * T * desc->k) + align_up(sizeof(float) * T * desc->d);
 }
 
+// The host-buffer layer overlaps its transfers with compute where the call's
+// order allows (x is 168 MB in and out 168 MB back at 16,384 tokens; the
+// link moves about 200 GB/s, about 0.85 ms each way):
+//  - x is copied on a copy stream of its own, which waits only until the
+//    previous call's q8 step has read the staging buffer: a call enqueued
+//    while the previous one computes brings its x in behind those products
+//    (when the previous call used another staging buffer, the copy waits
+//    for everything enqueued on `stream` before this call instead);
+//  - the routing ids and weights (small) are copied on the caller's stream;
+//  - the combine runs in token chunks, and each chunk's rows of out go back
+//    on a second copy stream as soon as they are written; the caller's
+//    stream then waits for the last chunk, so out is complete once `stream`
+//    is.
+// Under stream capture, or without the copy streams, every copy runs on the
+// caller's stream in order.
+constexpr int kOutChunks = 8;
+
 int moe_prefill_layer_host(const MoeLayerDesc* desc, const float* h_x, const int32_t* h_ids,
                            const float* h_w, const uint8_t* weight_pack,
                            const int64_t* expert_offsets, float* h_out, void* io,
@@ -489,17 +519,63 @@ int moe_prefill_layer_host(const MoeLayerDesc* desc, const float* h_x, const int
   float* d_w = (float*)(p + align_up(bx) + align_up(bi));
   float* d_out = (float*)(p + align_up(bx) + align_up(bi) + align_up(bw));
   cudaStream_t st = (cudaStream_t)stream;
-  if (T > 0) {
-    if (cudaMemcpyAsync(d_x, h_x, bx, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-        cudaMemcpyAsync(d_ids, h_ids, bi, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-        cudaMemcpyAsync(d_w, h_w, bw, cudaMemcpyHostToDevice, st) != cudaSuccess)
+  if (T == 0) {
+    if ((rc = run_route(c, d_ids, st))) return rc;
+    return MOE_OK;
+  }
+  std::unique_lock<std::mutex> lock(g_side_mu);
+  SideStream* sd = side_stream(st);
+  const bool overlap = sd != nullptr;
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  if (overlap) {
+    cudaEvent_t guard = sd->x_free;
+    if (sd->last_io != io) {
+      guard = sd->entry;
+      if (!ok(cudaEventRecord(guard, st))) return MOE_ERR_LAUNCH;
+    }
+    if (!ok(cudaStreamWaitEvent(sd->h2d, guard, 0)) ||
+        !ok(cudaMemcpyAsync(d_x, h_x, bx, cudaMemcpyHostToDevice, sd->h2d)) ||
+        !ok(cudaEventRecord(sd->x_in, sd->h2d)))
+      return MOE_ERR_LAUNCH;
+  } else if (!ok(cudaMemcpyAsync(d_x, h_x, bx, cudaMemcpyHostToDevice, st))) {
+    return MOE_ERR_LAUNCH;
+  }
+  if (!ok(cudaMemcpyAsync(d_ids, h_ids, bi, cudaMemcpyHostToDevice, st)) ||
+      !ok(cudaMemcpyAsync(d_w, h_w, bw, cudaMemcpyHostToDevice, st)))
+    return MOE_ERR_LAUNCH;
+  lock.unlock();
+  if ((rc = run_route(c, d_ids, st))) return rc;
+  if (overlap && !ok(cudaStreamWaitEvent(st, sd->x_in, 0))) return MOE_ERR_LAUNCH;
+  if ((rc = run_quant(c, d_x, st))) return rc;
+  if (overlap) {
+    lock.lock();
+    const bool rec = ok(cudaEventRecord(sd->x_free, st));
+    sd->last_io = io;
+    lock.unlock();
+    if (!rec) return MOE_ERR_LAUNCH;
+  }
+  if ((rc = run_gemm(c, 0, weight_pack, expert_offsets, st, true))) return rc;
+  if (!overlap || (c.d.flags & MOE_FLAG_FUSED_COMBINE)) {
+    if ((rc = run_down_and_combine(c, weight_pack, expert_offsets, d_w, d_out, st))) return rc;
+    if (!ok(cudaMemcpyAsync(h_out, d_out, bx, cudaMemcpyDeviceToHost, st))) return MOE_ERR_LAUNCH;
+    return MOE_OK;
+  }
+  if ((rc = run_gemm(c, 1, weight_pack, expert_offsets, st))) return rc;
+  lock.lock();
+  const size_t row_bytes = sizeof(float) * c.d.d;
+  for (int ch = 0; ch < kOutChunks; ch++) {
+    const int64_t t0 = (int64_t)(T * ch / kOutChunks), t1 = (int64_t)(T * (ch + 1) / kOutChunks);
+    if (t1 == t0) continue;
+    if (!ok(launch_combine(d_w, c.v.dst_of, c.v.dm, t0, t1 - t0, c.d.k, c.d.d, rows_max(c.d),
+                           d_out, st)) ||
+        !ok(cudaEventRecord(sd->comb, st)) || !ok(cudaStreamWaitEvent(sd->d2h, sd->comb, 0)) ||
+        !ok(cudaMemcpyAsync(reinterpret_cast<uint8_t*>(h_out) + t0 * row_bytes,
+                            reinterpret_cast<uint8_t*>(d_out) + t0 * row_bytes,
+                            (t1 - t0) * row_bytes, cudaMemcpyDeviceToHost, sd->d2h)))
       return MOE_ERR_LAUNCH;
   }
-  if ((rc = run_route(c, d_ids, st))) return rc;
-  if ((rc = run_quant(c, d_x, st))) return rc;
-  if ((rc = run_gemm(c, 0, weight_pack, expert_offsets, st, true))) return rc;
-  if ((rc = run_down_and_combine(c, weight_pack, expert_offsets, d_w, d_out, st))) return rc;
-  if (T > 0 && cudaMemcpyAsync(h_out, d_out, bx, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+  if (!ok(cudaEventRecord(sd->out_done, sd->d2h)) ||
+      !ok(cudaStreamWaitEvent(st, sd->out_done, 0)))
     return MOE_ERR_LAUNCH;
   return MOE_OK;
 }

@@ -77,8 +77,10 @@ cudaError_t launch_quant_q8(const float* x, int64_t T, int K, int k, const int32
 // hq [rows_max x n_ff], dh [rows_max x scale_stride(n_ff)]
 cudaError_t launch_swiglu_quant(const float* gu, const int32_t* nrows_dev, int64_t rows_max,
                                 int n_ff, int gu_layout, __half* hq, float* dh, cudaStream_t st);
+// tokens [t0, t0 + T) of the combine; rows_max bounds dst_of's row indices
 cudaError_t launch_combine(const float* topk_w, const int32_t* dst_of, const float* dm,
-                           int64_t T, int k, int d, float* out, cudaStream_t st);
+                           int64_t t0, int64_t T, int k, int d, int64_t rows_max, float* out,
+                           cudaStream_t st);
 
 // ------------------------------------------------------------ products
 // The combine fused into the down product's epilogue (when out is set): the

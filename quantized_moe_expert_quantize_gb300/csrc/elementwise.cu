@@ -151,9 +151,8 @@ swiglu_quant_kernel(const float* __restrict__ gu, const int32_t* __restrict__ nr
 
 __global__ void __launch_bounds__(256)
 combine_kernel(const float* __restrict__ topk_w, const int32_t* __restrict__ dst_of,
-               const float4* __restrict__ dm, int64_t T, int k, int d4,
+               const float4* __restrict__ dm, int64_t T, int k, int d4, int64_t rows_max,
                float4* __restrict__ out) {
-  const int64_t rows_max = T * k;
   const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= T * d4) return;
   const int64_t t = g / d4;
@@ -221,12 +220,13 @@ cudaError_t launch_combine_init(const int32_t* dst_of, int64_t T, int k, int gro
 }
 
 cudaError_t launch_combine(const float* topk_w, const int32_t* dst_of, const float* dm,
-                           int64_t T, int k, int d, float* out, cudaStream_t st) {
+                           int64_t t0, int64_t T, int k, int d, int64_t rows_max, float* out,
+                           cudaStream_t st) {
   const int64_t n = T * (d / 4);
   if (n == 0) return cudaSuccess;
   combine_kernel<<<blocks_for(n, 256), 256, 0, st>>>(
-      topk_w, dst_of, reinterpret_cast<const float4*>(dm), T, k, d / 4,
-      reinterpret_cast<float4*>(out));
+      topk_w + t0 * k, dst_of + t0 * k, reinterpret_cast<const float4*>(dm), T, k, d / 4,
+      rows_max, reinterpret_cast<float4*>(out + t0 * d));
   count_launch();
   return cudaGetLastError();
 }

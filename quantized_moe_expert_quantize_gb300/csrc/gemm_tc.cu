@@ -129,8 +129,10 @@ static_assert(kOffBar % 8 == 0 && kOffEoff % 8 == 0 && kOffRaw % 16 == 0 && kOff
               "alignment");
 
 // What the epilogue writes: GU rows (gate/up), Hq and its scales (gate/up
-// with swiglu_quant fused), or Dm rows (down).
-constexpr int kModeGU = 0, kModeSwiglu = 1, kModeDown = 2;
+// with swiglu_quant fused), Dm rows (down), or Dm rows with the combine
+// fused (a mode of its own, so that the plain down kernel carries none of
+// its code).
+constexpr int kModeGU = 0, kModeSwiglu = 1, kModeDown = 2, kModeDownComb = 3;
 
 struct TcArgs {
   const uint8_t* pack;  // tiled weight pack
@@ -149,7 +151,6 @@ struct TcArgs {
   float* dh;            // fused swiglu_quant: scales [rows x scale_stride(N_out/2)]
   int64_t rows_max;
   int32_t* status;
-  CombineArgs comb;     // down: the combine fused into the epilogue (comb.out set)
 };
 
 struct Item {
@@ -348,9 +349,9 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, uint32_t n, uint32_t 
 template <int FMT, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
-               const __grid_constant__ CUtensorMap tmap_d) {
+               const __grid_constant__ CUtensorMap tmap_d, const CombineArgs comb) {
   constexpr bool kFold = (FMT == MOE_FMT_W2);
-  constexpr bool kDown = (MODE == kModeDown);
+  constexpr bool kDown = (MODE == kModeDown || MODE == kModeDownComb);
   constexpr int kBps = kFold ? 1 : 2;                  // weight blocks per stage
   constexpr int kCB = chunk_blocks(FMT);               // weight blocks per raw chunk
   constexpr int kCode = code_bytes(FMT);               // code bytes per (row, block)
@@ -531,10 +532,12 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
         float* outp = a.out + row * a.N_out + I.o0 + 64 * h;
 #pragma unroll
         for (int j = 0; j < 8; j++) st_global_v8(outp + 8 * j, acc + 4 * j);
-        if (a.comb.out) {
-          // this thread stored both 32-column groups of its row
-          combine_arrive(a.comb, a.out, a.rows_max, a.N_out, row, I.o0 + 64 * h);
-          combine_arrive(a.comb, a.out, a.rows_max, a.N_out, row, I.o0 + 64 * h + 32);
+        if (MODE == kModeDownComb) {
+          // this thread stored both 32-column groups of its row (the combine
+          // fused into the epilogue: a parameter of its own, so that the
+          // other products' arguments keep their layout)
+          combine_arrive(comb, a.out, a.rows_max, a.N_out, row, I.o0 + 64 * h);
+          combine_arrive(comb, a.out, a.rows_max, a.N_out, row, I.o0 + 64 * h + 32);
         }
       } else if (MODE == kModeGU) {
         // gate outputs 128t + 32h .. + 31, and the matching up outputs
@@ -843,7 +846,6 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
   a.gu_layout = g.gu_layout;
   a.rows_max = g.rows_max;
   a.status = g.status;
-  a.comb = g.comb;
 
   auto encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
@@ -869,21 +871,25 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
   const int64_t tiles_max = max_tiles(g.rows_max, g.E) * (int64_t)((g.N_out + kTN - 1) / kTN);
   const int grid = (int)std::min<int64_t>(std::min<int64_t>(tiles_max, device_sm_count()),
                                           kMaxGrid);
-  const int mode = g.which == 1 ? kModeDown : (g.hq ? kModeSwiglu : kModeGU);
+  const int mode = g.which == 1 ? (g.comb.out ? kModeDownComb : kModeDown)
+                                : (g.hq ? kModeSwiglu : kModeGU);
   cudaError_t e = cudaSuccess;
 #define MOE_LAUNCH_TC(F, M)                                                             \
   if ((e = prepare_kernel<F, M>()) != cudaSuccess) return e;                            \
-  gemm_tc_kernel<F, M><<<grid, kThreads, kSmemBytes, st>>>(a, tmap, tmap_d);
+  gemm_tc_kernel<F, M><<<grid, kThreads, kSmemBytes, st>>>(a, tmap, tmap_d, g.comb);
   if (g.fmt == MOE_FMT_W2) {
     if (mode == kModeDown) { MOE_LAUNCH_TC(MOE_FMT_W2, kModeDown) }
+    else if (mode == kModeDownComb) { MOE_LAUNCH_TC(MOE_FMT_W2, kModeDownComb) }
     else if (mode == kModeSwiglu) { MOE_LAUNCH_TC(MOE_FMT_W2, kModeSwiglu) }
     else { MOE_LAUNCH_TC(MOE_FMT_W2, kModeGU) }
   } else if (g.fmt == MOE_FMT_W4NL) {
     if (mode == kModeDown) { MOE_LAUNCH_TC(MOE_FMT_W4NL, kModeDown) }
+    else if (mode == kModeDownComb) { MOE_LAUNCH_TC(MOE_FMT_W4NL, kModeDownComb) }
     else if (mode == kModeSwiglu) { MOE_LAUNCH_TC(MOE_FMT_W4NL, kModeSwiglu) }
     else { MOE_LAUNCH_TC(MOE_FMT_W4NL, kModeGU) }
   } else {
     if (mode == kModeDown) { MOE_LAUNCH_TC(MOE_FMT_Q8_0, kModeDown) }
+    else if (mode == kModeDownComb) { MOE_LAUNCH_TC(MOE_FMT_Q8_0, kModeDownComb) }
     else if (mode == kModeSwiglu) { MOE_LAUNCH_TC(MOE_FMT_Q8_0, kModeSwiglu) }
     else { MOE_LAUNCH_TC(MOE_FMT_Q8_0, kModeGU) }
   }
