@@ -71,7 +71,8 @@ constexpr int kActBox = 64;                                  // values per activ
 constexpr int kOffBar = kSlots * kSlotBytes;
 constexpr int kOffMisc = kOffBar + 2 * kSlots * 8;
 // misc: abort flag (+0), W4NL table (+64), warp-pair barriers [2][kWarps/2]
-// (+128); then the warp-pair amax exchange [2][kWarps][kRows] fp32
+// (+128), the ring producer's state (+192); then the warp-pair amax exchange
+// [2][kWarps][kRows] fp32
 constexpr int kOffAmax = kOffMisc + 256;
 constexpr int kSmemBytes = kOffAmax + 2 * kWarps * kRows * 4 + 1024;  // + alignment slack
 constexpr uint64_t kTimeoutNs = 1000000000ull;
@@ -163,11 +164,37 @@ __device__ __forceinline__ uint32_t w4_pair(uint32_t wlo, uint32_t whi, int i,
   return (uint32_t)lut[(wlo >> (4 * i)) & 15u] | ((uint32_t)lut[(whi >> (4 * i)) & 15u] << 16);
 }
 
+// Shared-memory loads at 32-bit shared addresses (volatile: they read bytes
+// that a TMA wrote after the mbarrier wait before them).
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float lds_half_as_f32(uint32_t a) {
+  unsigned short h;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(a));
+  return __half2float(__ushort_as_half(h));
+}
+
 // One item's products: every chunk of the item's weight tile against its
 // (up to 8 * NNT) routed rows, accumulated per 32-value block in K order into
 // acc (m16 fragment mt = tile rows rbase[mt]..+15, n8 fragment nt).  Tile
 // rows past the tile's end compute garbage from in-slot bytes and are never
-// stored.
+// stored.  Every shared-memory address is a per-lane offset, fixed for the
+// item, plus a per-chunk base advanced once a block.
 template <int FMT, int NNT, typename Refill>
 __device__ __forceinline__ bool consume_item(const uint8_t* smem, uint64_t* full, uint64_t* empty,
                                              volatile int* s_abort, uint32_t& cc, int nchunks,
@@ -181,37 +208,48 @@ __device__ __forceinline__ bool consume_item(const uint8_t* smem, uint64_t* full
   constexpr int kVals = kCB * kBv;           // K values per chunk
   constexpr int kDxW = dx_width(FMT);        // scales per dx row in the slot
   constexpr int kQpb = kBv / 32;             // q8 blocks per weight block
+  constexpr uint32_t kBoxBytes = kRows * kActBox * 2;  // one 64-value activation box
   const int g = lane >> 2, cq = lane & 3;
+  // ldmatrix: lanes 8m..8m+7 give rows 0..7 of matrix m; matrix 2ks + hf is
+  // stored positions 8hf..8hf+7 of group 2qb + ks: 16-byte chunk m + 4(qb&1)
+  // of the row in box qb/2, before the 128-byte swizzle
+  const int lm = lane >> 3, lr = lane & 7;
+  const uint32_t bsw0 = (uint32_t)(lr * 128 + ((lm ^ lr) << 4));
+  const uint32_t bsw1 = (uint32_t)(lr * 128 + (((lm + 4) ^ lr) << 4));
+  // this lane's tile rows rbase[mt] + g (+8 for h = 1): code and scale offsets
+  const uint32_t rc0 = (uint32_t)((rbase[0] + g) * kCode), rc1 = (uint32_t)((rbase[1] + g) * kCode);
+  const uint32_t rs0 = (uint32_t)((rbase[0] + g) * 2), rs1 = (uint32_t)((rbase[1] + g) * 2);
+  const uint32_t dxl = (uint32_t)(2 * cq * kDxW * 4);  // routed row 2cq of the dx box
+  const uint32_t codes_step = (uint32_t)(nw * kCode), scales_step = (uint32_t)(nw * 2);
+  const uint32_t smem_s = smem_u32(smem);
   const float zero[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   for (int c = 0; c < nchunks; c++, cc++) {
     const uint32_t slot = cc % kSlots;
     if (!mbar_wait(&full[slot], (cc / kSlots) & 1, s_abort, kTimeoutNs, false)) return false;
-    const uint8_t* sp = smem + slot * kSlotBytes;
+    const uint32_t sp = smem_s + slot * kSlotBytes;
     const int nbc = min(kCB, bpr - c * kCB);
-    const uint16_t* scl = reinterpret_cast<const uint16_t*>(sp + nbc * nw * kCode);
     const int dxo = (c * (kVals / 32)) & 3;  // this chunk's first scale in the dx box
-    const uint8_t* act = sp + kRawBytes;  // [box][32 rows][128 B], 128-byte swizzle
-    const float* dxs = reinterpret_cast<const float*>(sp + kRawBytes + kActBytes);
+    uint32_t cj = sp;                                        // block j's code records
+    uint32_t sj = sp + (uint32_t)(nbc * nw * kCode);         // and fp16 scales
+    const uint32_t act = sp + kRawBytes;                     // [box][32 rows][128 B], swizzled
+    uint32_t dxj = sp + kRawBytes + kActBytes + dxl + (uint32_t)(dxo * 4);  // q8 block j*kQpb
 #pragma unroll 1
-    for (int j = 0; j < nbc; j++) {
+    for (int j = 0; j < nbc; j++, cj += codes_step, sj += scales_step, dxj += 4 * kQpb) {
       float dw[2][2];  // scale of weight block j, tile rows rbase+g / +8
-#pragma unroll
-      for (int mt = 0; mt < 2; mt++)
-#pragma unroll
-        for (int h = 0; h < 2; h++)
-          dw[mt][h] = __half2float(__ushort_as_half(scl[j * nw + rbase[mt] + g + 8 * h]));
+      dw[0][0] = lds_half_as_f32(sj + rs0);
+      dw[0][1] = lds_half_as_f32(sj + rs0 + 16);
+      dw[1][0] = lds_half_as_f32(sj + rs1);
+      dw[1][1] = lds_half_as_f32(sj + rs1 + 16);
 #pragma unroll
       for (int qq = 0; qq < kQpb; qq++) {
         const int qb = j * kQpb + qq;  // q8 block within the chunk
-        // B fragments, one ldmatrix.x4 per n8 fragment: matrix 2ks + hf is
-        // routed rows 8nt..8nt+7 at stored positions 8hf..8hf+7 of group
-        // 2qb + ks (16-byte chunk 2*((2qb+ks)%4) + hf of box qb/2, 128-byte
-        // swizzle), so lane (g, cq) receives b[ks][nt][hf]
+        // B fragments, one ldmatrix.x4 per n8 fragment (routed rows
+        // 8nt..8nt+7): lane (g, cq) receives b[ks][nt][hf]
         uint32_t b[2][NNT][2];
         float dx[NNT][2];  // activation scales of routed rows 8nt + 2cq, +1
-        const int lm = lane >> 3, lr = lane & 7;  // this lane's matrix and row
-        const uint32_t bsrc = smem_u32(act + (qb >> 1) * (kRows * kActBox * 2) + lr * 128 +
-                                       (((2 * ((2 * qb + (lm >> 1)) & 3) + (lm & 1)) ^ lr) << 4));
+        const uint32_t bsrc =
+            kQpb == 2 ? act + (uint32_t)j * kBoxBytes + (qq ? bsw1 : bsw0)
+                      : act + (uint32_t)(qb >> 1) * kBoxBytes + ((qb & 1) ? bsw1 : bsw0);
 #pragma unroll
         for (int nt = 0; nt < NNT; nt++) {
           ldsm_x4(bsrc + nt * 8 * 128, b[0][nt][0], b[0][nt][1], b[1][nt][0], b[1][nt][1]);
@@ -219,19 +257,20 @@ __device__ __forceinline__ bool consume_item(const uint8_t* smem, uint64_t* full
             b[0][nt][1] = hmul2_u32(b[0][nt][1], kHalfInv256);
             b[1][nt][1] = hmul2_u32(b[1][nt][1], kHalfInv256);
           }
-          dx[nt][0] = dxs[(8 * nt + 2 * cq) * kDxW + dxo + qb];
-          dx[nt][1] = dxs[(8 * nt + 2 * cq + 1) * kDxW + dxo + qb];
+          dx[nt][0] = lds_f32(dxj + 4 * qq + nt * 8 * kDxW * 4);
+          dx[nt][1] = lds_f32(dxj + 4 * qq + nt * 8 * kDxW * 4 + kDxW * 4);
         }
 #pragma unroll
         for (int mt = 0; mt < 2; mt++) {
           // A fragments of both 16-value groups of the block
           uint32_t af[2][4];
+          const uint32_t wrow = cj + (mt ? rc1 : rc0);
 #pragma unroll
           for (int h = 0; h < 2; h++) {
-            const uint8_t* wrow = sp + (j * nw + rbase[mt] + g + 8 * h) * kCode;
+            const uint32_t wr = wrow + h * 8 * kCode;
             if (kW2) {
               // code words of groups 2qq, 2qq+1 of the block
-              const uint2 w = *reinterpret_cast<const uint2*>(wrow + 8 * qq);
+              const uint2 w = lds64(wr + 8 * qq);
               const uint32_t ws0 = w.x >> (2 * cq), ws1 = w.y >> (2 * cq);
               af[0][h] = w2_pair_lo(ws0);
               af[0][2 + h] = w2_pair_hi(ws0);
@@ -240,15 +279,14 @@ __device__ __forceinline__ bool consume_item(const uint8_t* smem, uint64_t* full
             } else if (FMT == MOE_FMT_Q8_0) {
               // group ks = words 4ks..4ks+3: values cq, cq+8 in words 4ks, 4ks+2
               // and cq+4, cq+12 in words 4ks+1, 4ks+3, byte cq of each
-              const uint4 w0 = reinterpret_cast<const uint4*>(wrow)[0];
-              const uint4 w1 = reinterpret_cast<const uint4*>(wrow)[1];
+              const uint4 w0 = lds128(wr), w1 = lds128(wr + 16);
               const uint32_t sel = (uint32_t)(cq | (cq << 4) | ((4 + cq) << 8) | ((4 + cq) << 12));
               af[0][h] = q8_pair(w0.x, w0.z, sel);
               af[0][2 + h] = q8_pair(w0.y, w0.w, sel);
               af[1][h] = q8_pair(w1.x, w1.z, sel);
               af[1][2 + h] = q8_pair(w1.y, w1.w, sel);
             } else {
-              const uint4 w = *reinterpret_cast<const uint4*>(wrow);
+              const uint4 w = lds128(wr);
               af[0][h] = w4_pair(w.x, w.y, cq, s_lut);
               af[0][2 + h] = w4_pair(w.x, w.y, cq + 4, s_lut);
               af[1][h] = w4_pair(w.z, w.w, cq, s_lut);
@@ -323,6 +361,7 @@ __device__ __forceinline__ void prod_seek(Producer& p, const SmArgs& a, int firs
     return;
   }
 }
+static_assert(sizeof(Producer) <= 64 && alignof(Producer) <= 64, "producer state fits its slot");
 template <int FMT>
 __device__ __forceinline__ void prod_issue(Producer& p, uint8_t* smem, uint64_t* full,
                                            const SmArgs& a, const CUtensorMap* tmap,
@@ -393,10 +432,12 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
 
   // ring: prefill every slot, then lane 0 of warp 0 refills a slot as soon
   // as all warps have released it
-  Producer prod;
-  prod.item = blockIdx.x;
-  prod.issued = 0;
+  // (its state lives in shared memory: only thread 0 touches it, and as
+  // registers it would be held by every thread of the CTA)
+  Producer& prod = *reinterpret_cast<Producer*>(smem + kOffMisc + 192);
   if (tid == 0) {
+    prod.item = blockIdx.x;
+    prod.issued = 0;
     prefetch_tmap(&tmap);
     prefetch_tmap(&tmap_d);
     prod_seek(prod, a, first, total, n_wtiles, mbytes);
@@ -461,6 +502,7 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
         for (int mt = 0; mt < 2; mt++) {
 #pragma unroll
           for (int nt = 0; nt < 4; nt++) {
+            if (nt >= nnt) break;
 #pragma unroll
             for (int i = 0; i < 4; i++) {
               const int rr = 8 * nt + 2 * cq + (i & 1);
@@ -488,7 +530,7 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
 #pragma unroll
           for (int i = 0; i < 4; i++) {
             const int rr = 8 * nt + 2 * cq + (i & 1);
-            if (rr < u) {
+            if (nt < nnt && rr < u) {
               const int oo = o + 8 * (i >> 1);
               float* orow = a.out + (int64_t)(t.y + rr) * a.N_out;
               if (inter) {
@@ -517,7 +559,8 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
         float hv[4][2][2];  // [nt][col][output g / g+8]
         float am[4][2];
 #pragma unroll
-        for (int nt = 0; nt < 4; nt++)
+        for (int nt = 0; nt < 4; nt++) {
+          if (nt >= nnt) break;
 #pragma unroll
           for (int col = 0; col < 2; col++) {
             float amax = 0.0f;
@@ -534,12 +577,14 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
             am[nt][col] = amax;
             if (g == 0) am_own[8 * nt + 2 * cq + col] = amax;
           }
+        }
         uint64_t* pb = &pairbar[xb * (kWarps / 2) + (warp >> 1)];
         mbar_arrive(pb);
         if (!(alive = mbar_wait(pb, (xc >> 1) & 1, s_abort, kTimeoutNs, false))) break;
         xc++;
 #pragma unroll
-        for (int nt = 0; nt < 4; nt++)
+        for (int nt = 0; nt < 4; nt++) {
+          if (nt >= nnt) break;
 #pragma unroll
           for (int col = 0; col < 2; col++) {
             const int rr = 8 * nt + 2 * cq + col;
@@ -553,6 +598,7 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
                 a.dh[(int64_t)(t.y + rr) * scale_stride(n_ff) + (o >> 5)] = d;
             }
           }
+        }
       }
     }
   }
