@@ -242,6 +242,7 @@ int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaSt
   a.pack_bytes = c.d.weight_pack_bytes;
   a.tiles = (const int4*)(c.ws + c.L.tiles);
   a.ntiles = c.v.status + 1;
+  a.sched = c.v.status + 4 + 2 * which;  // zeroed by routing (ntiles[3..6])
   a.E = c.d.E;
   a.status = c.v.status;
   a.rows_max = rows_max(c.d);

@@ -115,6 +115,7 @@ struct GemmArgs {
   float* dh;                 //   are written instead of GU
   int64_t rows_max;          // capacity of the routed-row buffers (T*k)
   int32_t* status;
+  int32_t* sched;            // small-row launch: {next item, CTAs done}, zeroed by routing
   CombineArgs comb;          // down only: the combine fused into the epilogue
 };
 

@@ -74,7 +74,17 @@ constexpr int kOffMisc = kOffBar + 2 * kSlots * 8;
 // (+128), the ring producer's state (+192); then the warp-pair amax exchange
 // [2][kWarps][kRows] fp32
 constexpr int kOffAmax = kOffMisc + 256;
-constexpr int kSmemBytes = kOffAmax + 2 * kWarps * kRows * 4 + 1024;  // + alignment slack
+// the dp4a path (W2 tiles of at most kDp4aRows rows, see item_dp4a): the
+// chunk's activations as int8 words [2 buffers][kDp4aRows rows][64 words],
+// their 32-value sums [2][kDp4aRows][8], the up rows of the fused
+// swiglu_quant [kDp4aRows][128] fp32, and its mbarriers (chunk buffers [2],
+// up exchange)
+constexpr int kDp4aRows = 4;
+constexpr int kOffConv = kOffAmax + 2 * kWarps * kRows * 4;
+constexpr int kOffConvSum = kOffConv + 2 * kDp4aRows * 64 * 4;
+constexpr int kOffUp = kOffConvSum + 2 * kDp4aRows * 8 * 4;
+constexpr int kOffDbar = kOffUp + kDp4aRows * (kTN / 2) * 4;
+constexpr int kSmemBytes = kOffDbar + 64 + 1024;  // + alignment slack
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 constexpr int kModeGU = 0, kModeSwiglu = 1, kModeDown = 2;
 static_assert(kSlotBytes % 1024 == 0 && kRawBytes % 1024 == 0, "swizzled boxes 1024-byte aligned");
@@ -99,6 +109,7 @@ struct SmArgs {
   float* dh;
   int64_t rows_max;
   int32_t* status;
+  int32_t* sched;    // {next item, CTAs done}: zero at launch (see prod_seek)
   CombineArgs comb;  // down: the combine fused into the epilogue (comb.out set)
 };
 
@@ -318,6 +329,192 @@ __device__ __forceinline__ bool consume_item(const uint8_t* smem, uint64_t* full
   return true;
 }
 
+__device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// One W2 item of U <= kDp4aRows routed rows on the integer dot-product
+// units instead of the tensor cores.  With so few rows an m16n8k16 MMA is at
+// most half used (its N side is 8 rows) and each lane still decodes its
+// share of every weight value into fp16; dp4a takes four 2-bit codes, each
+// in a byte, against four int8 activations, so a code word decodes with a
+// shift and a mask per four values and no fp16 step.
+//
+// Thread tid owns tile row tid (gate/up: gate rows below nw/2, the matching
+// up rows above; down: output column 256*wt + tid).  Per chunk the CTA first
+// turns the U activation rows of the slot (fp16 integers, stored
+// pair-interleaved and 128-byte swizzled) into int8 words in the order the
+// codes come out of a word -- word s of group G holds values 16G + s, +4, +8,
+// +12 -- together with each 32-value block's sum of q (one word per thread,
+// all warps, an mbarrier of all warps publishes them; two buffers by chunk).
+// Then each thread, per 64-value W2 block of its row: the four code words,
+// each shifted by 2s and masked to bytes (c in 0..3), dp4a against the
+// activation words of every row; per 32-value block the exact integer
+// isum = sum(c q) - 2 sum(q) = sum((c - 2) q), and the same epilogue as the
+// tensor-core paths, acc += d_x * (d_w * isum) with d_w * isum exact: the
+// bits equal the m16n8k16 path's.
+template <int MODE, int U, typename Refill>
+__device__ __forceinline__ bool item_dp4a(const SmArgs& a, const uint8_t* smem, uint64_t* full,
+                                          uint64_t* empty, uint64_t* cbar, uint64_t* ubar,
+                                          volatile int* s_abort, uint32_t& cc, uint32_t& dc,
+                                          uint32_t& uc, int nchunks, int nw, int4 t, int wt,
+                                          Refill&& refill) {
+  constexpr int kCB = chunk_blocks(MOE_FMT_W2);  // 4 W2 blocks (256 values) a chunk
+  constexpr int kCode = code_bytes(MOE_FMT_W2);  // 16
+  constexpr int kDxW = dx_width(MOE_FMT_W2);     // 8 scales a row of the dx box
+  constexpr uint32_t kBoxBytes = kRows * kActBox * 2;
+  static_assert(kCB * 64 == kChunkVals && kDxW == 8, "a W2 chunk is 8 q8 blocks");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t smem_s = smem_u32(smem);
+  const uint32_t conv_s = smem_s + kOffConv, csum_s = smem_s + kOffConvSum;
+  float acc[U];
+#pragma unroll
+  for (int r = 0; r < U; r++) acc[r] = 0.0f;
+  for (int c = 0; c < nchunks; c++, cc++, dc++) {
+    const uint32_t slot = cc % kSlots;
+    if (!mbar_wait(&full[slot], (cc / kSlots) & 1, s_abort, kTimeoutNs, false)) return false;
+    const uint32_t sp = smem_s + slot * kSlotBytes;
+    const int nbc = min(kCB, a.bpr - c * kCB);
+    const uint32_t buf = dc & 1;
+    const uint32_t words = conv_s + buf * (kDp4aRows * 64 * 4);  // [row][64]
+    const uint32_t sums = csum_s + buf * (kDp4aRows * 8 * 4);    // [row][8]
+    // ---- the chunk's activation words: thread tid < 64U makes word tid
+    // (row tid/64, group G, shift s) from stored words 8G+s (values s, s+8)
+    // and 8G+s+4 (values s+4, s+12); 1536 + q in fp16 has q's two's
+    // complement in its low byte
+    {
+      int qsum = 0;
+      if (tid < 64 * U) {  // whole warps
+        const int r = tid >> 6, jj = tid & 63, G = jj >> 2, sh = jj & 3;
+        const int w0 = 8 * G + sh, w1 = w0 + 4;
+        const uint32_t row = sp + kRawBytes + (uint32_t)(r * 128);
+        const uint32_t x = lds32(row + (uint32_t)(w0 >> 5) * kBoxBytes +
+                                 ((((w0 & 31) >> 2) ^ (r & 7)) << 4) + (w0 & 3) * 4);
+        const uint32_t y = lds32(row + (uint32_t)(w1 >> 5) * kBoxBytes +
+                                 ((((w1 & 31) >> 2) ^ (r & 7)) << 4) + (w1 & 3) * 4);
+        const uint32_t word = __byte_perm(hadd2_u32(x, 0x66006600u), hadd2_u32(y, 0x66006600u),
+                                          0x6240);
+        sts32(words + (uint32_t)(r * 256 + jj * 4), word);
+        qsum = __dp4a((int)word, 0x01010101, 0);
+      }
+      // a q8 block is 8 consecutive words: lanes 8m .. 8m+7
+      qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+      qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+      qsum += __shfl_xor_sync(0xffffffffu, qsum, 4);
+      if (tid < 64 * U && (tid & 7) == 0)
+        sts32(sums + (uint32_t)((tid >> 6) * 32 + ((tid & 63) >> 3) * 4), (uint32_t)qsum);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cbar[buf]);
+      if (!mbar_wait(&cbar[buf], (dc >> 1) & 1, s_abort, kTimeoutNs, false)) return false;
+    }
+    // ---- this thread's row against the U rows
+    const uint32_t dxs = sp + kRawBytes + kActBytes;  // [32 rows][8] fp32 (this chunk's 8 blocks)
+    uint32_t cj = sp + (uint32_t)(tid * kCode);                       // codes of (block j, row tid)
+    uint32_t sj = sp + (uint32_t)(nbc * nw * kCode) + (uint32_t)(tid * 2);  // its fp16 scale
+#pragma unroll 1
+    for (int j = 0; j < nbc; j++, cj += nw * kCode, sj += nw * 2) {
+      const uint4 w4 = lds128(cj);
+      const float dw = lds_half_as_f32(sj);
+      const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};  // groups 4j .. 4j+3
+      uint32_t cw[4][4];                                 // [group][shift]: codes as bytes
+#pragma unroll
+      for (int g = 0; g < 4; g++)
+#pragma unroll
+        for (int sh = 0; sh < 4; sh++) cw[g][sh] = (wv[g] >> (2 * sh)) & 0x03030303u;
+#pragma unroll
+      for (int r = 0; r < U; r++) {
+        int isum[2] = {0, 0};  // q8 blocks 2j, 2j+1
+#pragma unroll
+        for (int g = 0; g < 4; g++) {
+          const uint4 av = lds128(words + (uint32_t)(r * 256 + 64 * j + 16 * g));
+          isum[g >> 1] = __dp4a((int)cw[g][0], (int)av.x, isum[g >> 1]);
+          isum[g >> 1] = __dp4a((int)cw[g][1], (int)av.y, isum[g >> 1]);
+          isum[g >> 1] = __dp4a((int)cw[g][2], (int)av.z, isum[g >> 1]);
+          isum[g >> 1] = __dp4a((int)cw[g][3], (int)av.w, isum[g >> 1]);
+        }
+#pragma unroll
+        for (int qq = 0; qq < 2; qq++) {
+          const int qb = 2 * j + qq;
+          const int qs = (int)lds32(sums + (uint32_t)(r * 32 + qb * 4));
+          const float dx = lds_f32(dxs + (uint32_t)((r * kDxW + qb) * 4));
+          acc[r] = __fmaf_rn(dx, __fmul_rn(dw, (float)(isum[qq] - 2 * qs)), acc[r]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+    refill(cc);
+  }
+
+  // ---- the item's outputs
+  if (MODE == kModeDown) {
+    if (tid < nw) {
+#pragma unroll
+      for (int r = 0; r < U; r++) a.out[(int64_t)(t.y + r) * a.N_out + wt * kTN + tid] = acc[r];
+    }
+    if (a.comb.out && 32 * warp < nw) {
+      // the warp stored the 32-column group 32w .. 32w+31 of every routed
+      // row of the tile; one lane per row counts it in
+      __syncwarp();
+      if (lane < U)
+        combine_arrive(a.comb, a.out, a.rows_max, a.N_out, (int64_t)t.y + lane, wt * kTN + 32 * warp);
+    }
+    return true;
+  }
+  const int n_ff = a.N_out >> 1, nwg = nw >> 1;
+  if (MODE == kModeGU) {
+    if (tid < nw) {
+      const bool up = tid >= nwg;
+      const int o = wt * (kTN / 2) + (up ? tid - nwg : tid);
+      const int col = a.gu_layout == MOE_GU_INTERLEAVED ? 2 * o + (up ? 1 : 0) : (up ? n_ff : 0) + o;
+#pragma unroll
+      for (int r = 0; r < U; r++) a.out[(int64_t)(t.y + r) * a.N_out + col] = acc[r];
+    }
+    return true;
+  }
+  // swiglu_quant fused: the up threads hand their rows to the gate threads
+  // through shared memory; a gate warp then holds 32 consecutive outputs of
+  // H, one q8 block, per routed row
+  float* s_up = reinterpret_cast<float*>(const_cast<uint8_t*>(smem) + kOffUp);
+  if (tid >= nwg && tid < nw) {
+#pragma unroll
+    for (int r = 0; r < U; r++) s_up[r * (kTN / 2) + tid - nwg] = acc[r];
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(ubar);
+  if (!mbar_wait(ubar, uc & 1, s_abort, kTimeoutNs, false)) return false;
+  uc++;
+  if (tid < nwg) {  // whole warps: nwg is a multiple of 32
+    const int o = wt * (kTN / 2) + tid;
+    // stored position of output o in its 16-value group (pair-interleaved)
+    const int i16 = o & 15;
+    const int pos = (o & ~15) + (i16 < 8 ? 2 * i16 : 2 * (i16 - 8) + 1);
+#pragma unroll
+    for (int r = 0; r < U; r++) {
+      const float gv = acc[r], uv = s_up[r * (kTN / 2) + tid];
+      const float hv = __fmul_rn(__fdiv_rn(gv, __fadd_rn(1.0f, expf(-gv))), uv);
+      float amax = fabsf(hv);
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+      const float d = __fdiv_rn(amax, 127.0f);
+      const float q = (d == 0.0f) ? 0.0f : rintf(__fdiv_rn(hv, d));
+      a.hq[(int64_t)(t.y + r) * n_ff + pos] = __float2half_rn(q);
+      if (lane == 0) a.dh[(int64_t)(t.y + r) * scale_stride(n_ff) + (o >> 5)] = d;
+    }
+  }
+  return true;
+}
+
 // One item (small-row tile x 256-row weight tile) of the work list, checked.
 struct ItemInfo {
   int4 t;        // {expert, first routed row, rows, -}
@@ -338,6 +535,16 @@ __device__ __forceinline__ ItemInfo item_info(const SmArgs& a, int first, int n_
   return I;
 }
 
+// Work distribution: the producer of every CTA takes the next item of the
+// work list from a counter in global memory (a.sched[0]), so a CTA that
+// drew cheap items draws more.  Items differ in cost several times over (an
+// m16n8k16 item of 17-32 rows against a dp4a item of one row), and with a
+// fixed round-robin deal the multiprocessors sat idle a fifth of the time
+// at 128 tokens.  The producer writes each chunk's item into s_item[slot]
+// before it arms the slot; after the list it arms one more slot with no
+// copies and item -1, which ends the consumers' loop.  routing zeroes the
+// counters, and the last CTA to finish zeroes them again for the next launch.
+//
 // The load side of the ring (lane 0 of warp 0): the next (item, chunk) to
 // load, in the order the warps consume them.  Per chunk: one bulk copy of
 // the raw weight chunk and the tile's activation rows and scales in 2-D TMA
@@ -347,12 +554,21 @@ struct Producer {
   const uint8_t* wbase;
   int row0, nw, nbox;
   uint32_t issued;
+  int ended;    // the closing slot is armed
 };
 __device__ __forceinline__ void prod_seek(Producer& p, const SmArgs& a, int first, int total,
                                           int n_wtiles, int64_t mbytes) {
-  for (; p.item < total; p.item += gridDim.x) {
+  for (;;) {
+    p.item = atomicAdd(a.sched, 1);
+    if (p.item >= total) {
+      p.item = total;
+      return;
+    }
     const ItemInfo I = item_info(a, first, n_wtiles, mbytes, p.item);
-    if (!I.ok) continue;
+    if (!I.ok) {
+      atomicOr(a.status, MOE_STATUS_BAD_OFFSET);
+      continue;
+    }
     p.c = 0;
     p.row0 = I.t.y;
     p.nw = I.nw;
@@ -361,7 +577,7 @@ __device__ __forceinline__ void prod_seek(Producer& p, const SmArgs& a, int firs
     return;
   }
 }
-static_assert(sizeof(Producer) <= 64 && alignof(Producer) <= 64, "producer state fits its slot");
+static_assert(sizeof(Producer) <= 48 && alignof(Producer) <= 16, "producer state fits its slot");
 template <int FMT>
 __device__ __forceinline__ void prod_issue(Producer& p, uint8_t* smem, uint64_t* full,
                                            const SmArgs& a, const CUtensorMap* tmap,
@@ -371,6 +587,15 @@ __device__ __forceinline__ void prod_issue(Producer& p, uint8_t* smem, uint64_t*
   constexpr int kVals = kCB * block_values(FMT);
   constexpr int kDxW = dx_width(FMT);
   const uint32_t slot = p.issued % kSlots;
+  volatile int* s_item = reinterpret_cast<volatile int*>(smem + kOffMisc + 240);
+  if (p.item >= total) {  // the closing slot: no copies, item -1
+    s_item[slot] = -1;
+    mbar_arrive(&full[slot]);
+    p.ended = 1;
+    p.issued++;
+    return;
+  }
+  s_item[slot] = p.item;
   uint8_t* sp = smem + slot * kSlotBytes;
   const int nbc = min(kCB, a.bpr - p.c * kCB);
   const uint32_t raw = (uint32_t)(nbc * p.nw * kBB);
@@ -386,10 +611,7 @@ __device__ __forceinline__ void prod_issue(Producer& p, uint8_t* smem, uint64_t*
                 (p.c * (kVals / 32)) & ~3, p.row0 + kBoxRows * hb, &full[slot]);
   }
   p.issued++;
-  if (++p.c == nchunks) {
-    p.item += gridDim.x;
-    prod_seek(p, a, first, total, n_wtiles, mbytes);
-  }
+  if (++p.c == nchunks) prod_seek(p, a, first, total, n_wtiles, mbytes);
 }
 
 template <int FMT, int MODE>
@@ -409,6 +631,7 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
   uint16_t* s_lut = reinterpret_cast<uint16_t*>(smem + kOffMisc + 64);
   uint64_t* pairbar = reinterpret_cast<uint64_t*>(smem + kOffMisc + 128);
   float* s_amax = reinterpret_cast<float*>(smem + kOffAmax);
+  uint64_t* cbar = reinterpret_cast<uint64_t*>(smem + kOffDbar);  // [2], then the up exchange
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -417,6 +640,7 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
       mbar_init(&empty[i], kWarps);
     }
     for (int i = 0; i < kWarps; i++) mbar_init(&pairbar[i], 64);  // both warps of a pair
+    for (int i = 0; i < 3; i++) mbar_init(&cbar[i], kWarps);      // lane 0 of every warp
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -435,18 +659,19 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
   // (its state lives in shared memory: only thread 0 touches it, and as
   // registers it would be held by every thread of the CTA)
   Producer& prod = *reinterpret_cast<Producer*>(smem + kOffMisc + 192);
+  volatile int* s_item = reinterpret_cast<volatile int*>(smem + kOffMisc + 240);
   if (tid == 0) {
-    prod.item = blockIdx.x;
     prod.issued = 0;
+    prod.ended = 0;
     prefetch_tmap(&tmap);
     prefetch_tmap(&tmap_d);
     prod_seek(prod, a, first, total, n_wtiles, mbytes);
-    for (int s = 0; s < kSlots && prod.item < total; s++)
+    for (int s = 0; s < kSlots && !prod.ended; s++)
       prod_issue<FMT>(prod, smem, full, a, &tmap, &tmap_d, first, total, n_wtiles, mbytes, nchunks);
   }
   auto refill = [&](uint32_t done) {  // chunk `done` was consumed by this warp
     if (warp == 0) {
-      if (lane == 0 && prod.item < total) {
+      if (lane == 0 && !prod.ended) {
         // all warps released chunk `done`'s slot: load the chunk kSlots ahead
         if (mbar_wait(&empty[done % kSlots], (done / kSlots) & 1, s_abort, kTimeoutNs, false))
           prod_issue<FMT>(prod, smem, full, a, &tmap, &tmap_d, first, total, n_wtiles, mbytes,
@@ -459,15 +684,32 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
   const int g = lane >> 2, cq = lane & 3;
   uint32_t cc = 0;
   uint32_t xc = 0;  // amax exchanges of this warp's pair so far
+  uint32_t dc = 0;  // chunks of dp4a items so far (their conversion buffers)
+  uint32_t uc = 0;  // up-row exchanges of dp4a items so far
   bool alive = true;
-  for (int item = blockIdx.x; item < total && alive; item += gridDim.x) {
+  while (alive) {
+    // the next item is the one the producer put in the next slot
+    if (!(alive = mbar_wait(&full[cc % kSlots], (cc / kSlots) & 1, s_abort, kTimeoutNs, false)))
+      break;
+    const int item = s_item[cc % kSlots];
+    if (item < 0) break;  // the closing slot
     const ItemInfo I = item_info(a, first, n_wtiles, mbytes, item);
-    if (!I.ok) {
-      if (tid == 0) atomicOr(a.status, MOE_STATUS_BAD_OFFSET);
-      continue;
-    }
     const int4 t = I.t;
     const int wt = I.wt, nw = I.nw;
+    if constexpr (kW2) {
+      if (t.z <= kDp4aRows) {
+#define MOE_SMALL_DP4A(N)                                                                       \
+  item_dp4a<MODE, N>(a, smem, full, empty, cbar, cbar + 2, s_abort, cc, dc, uc, nchunks, nw, t, wt, \
+                     refill)
+        alive = t.z == 1   ? MOE_SMALL_DP4A(1)
+                : t.z == 2 ? MOE_SMALL_DP4A(2)
+                : t.z == 3 ? MOE_SMALL_DP4A(3)
+                           : MOE_SMALL_DP4A(4);
+#undef MOE_SMALL_DP4A
+        if (!alive) break;
+        continue;
+      }
+    }
     {
       const int u = t.z;
       const int nnt = (u + 7) >> 3;  // n8 fragments of routed rows (1 to 4)
@@ -607,6 +849,16 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
     for (uint32_t i = cc; i < prod.issued; i++)
       if (!mbar_wait(&full[i % kSlots], (i / kSlots) & 1, s_abort, kTimeoutNs, false)) break;
   if (*s_abort && tid == 0) atomicOr(a.status, MOE_STATUS_PIPE_TIMEOUT);
+  // the last CTA to finish (every producer has taken its last item) zeroes
+  // the work counter for the next launch
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(a.sched + 1, 1) == (int)gridDim.x - 1) {
+      a.sched[0] = 0;
+      a.sched[1] = 0;
+      __threadfence();
+    }
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_small() {
@@ -680,6 +932,7 @@ cudaError_t launch_gemm_small(const GemmArgs& g, cudaStream_t st) {
   a.dh = g.dh;
   a.rows_max = g.rows_max;
   a.status = g.status;
+  a.sched = g.sched;
   a.comb = g.comb;
 
   auto encode = get_encode_small();

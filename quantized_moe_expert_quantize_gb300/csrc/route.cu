@@ -140,6 +140,9 @@ __device__ __forceinline__ int expert_lists(int run, int E, int32_t* __restrict_
     sh.tot[1] = sbase + ns;
     ntiles[0] = tbase + nt + sbase + ns;
     ntiles[1] = tbase + nt;  // the tcgen05 tiles come first
+    // the small-row launches' work counters ({next item, CTAs done} for
+    // gate/up, then for down) start at zero
+    ntiles[3] = ntiles[4] = ntiles[5] = ntiles[6] = 0;
   }
   __syncthreads();
   sh.tiles[tid] = tbase;
@@ -353,8 +356,9 @@ namespace {
 constexpr int64_t kNoAllocScratchInts = 1 << 18;  // 1 MiB of int32
 static __device__ __align__(256) int32_t g_route_scratch[kNoAllocScratchInts];
 
-// layout in ints: [0] status bits, [1..2] the tile counts, [64..] expert
-// order, then the tile list (int4), then the chunk histogram
+// layout in ints: [0] status bits, [1..2] the tile counts ([4..7] zeroed with
+// them), [64..] expert order, then the tile list (int4), then the chunk
+// histogram
 struct NoAllocLayout {
   int64_t order, tiles, hist, total;
 };
