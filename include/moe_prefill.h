@@ -314,8 +314,9 @@ int moe_read_status(const MoeLayerDesc *desc, void *workspace,
  *                                  expert id is outside [0, E)
  * Its scratch is a fixed 1 MiB array in the library's device memory (held by
  * every GPU that loads the library until the process exits) instead of a
- * workspace: ceil(T*k/1024)*E + 4*floor(T*k/128) + 9*E + 71 int32 must fit
- * in 262144 (T*k = 163840 with E = 512 needs about 92,000), or
+ * workspace: (c + ceil(c/8))*E + 4*floor(T*k/128) + 9*E + 71 int32, with
+ * c = ceil(T*k/1024), must fit in 262144 (T*k = 163840 with E = 512 needs
+ * about 102,000), or
  * MOE_ERR_SCRATCH is returned with nothing enqueued.  Every call looks the
  * array's device address up (cudaGetSymbolAddress) with the current device
  * current; the first call on a device also loads the library's device code

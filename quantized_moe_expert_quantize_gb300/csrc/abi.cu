@@ -89,7 +89,7 @@ Layout layout(const MoeLayerDesc& d) {
   L.tiles = take(sizeof(int4) * (size_t)max_tiles(R, d.E));
   L.row_src = take(sizeof(int32_t) * R);
   L.dst_of = take(sizeof(int32_t) * R);
-  L.hist = take(sizeof(int32_t) * (size_t)nchunks * d.E);
+  L.hist = take(sizeof(int32_t) * (size_t)route_hist_rows(R) * d.E);
   L.xq = take(sizeof(uint16_t) * (size_t)R * d.d);
   L.dx = take(sizeof(float) * (size_t)R * scale_stride(d.d));
   L.gu = take(sizeof(float) * (size_t)R * 2 * d.n_ff);

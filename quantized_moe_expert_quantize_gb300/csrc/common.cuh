@@ -45,6 +45,12 @@ void count_launch(int n = 1);
 constexpr int kRouteChunk = 1024;  // flat entries per warp
 constexpr int kRouteWarps = 8;     // warps per CTA
 inline int route_chunks(int64_t n) { return (int)((n + kRouteChunk - 1) / kRouteChunk); }
+// rows of E int32 the multi-launch routing keeps: one per chunk (the chunk's
+// first row in each expert within its CTA), then one per CTA of chunks
+inline int64_t route_hist_rows(int64_t n) {
+  const int c = route_chunks(n);
+  return (int64_t)c + (c + kRouteWarps - 1) / kRouteWarps;
+}
 
 // Routed-row tiles of the product kernels.  Every expert's rows are cut
 // into tiles of kTileRows rows for the tcgen05 kernel; what is left after

@@ -9,8 +9,10 @@
 // saved matters more there than parallelism.  Beyond that, three kernels:
 //   1. route_hist    -- one warp per chunk of 1024 flat entries counts the
 //                       chunk's rows per expert (shared-memory histogram);
-//   2. route_scan    -- one CTA turns the [chunk][expert] counts into the
-//                       base row of every (chunk, expert), the expert counts,
+//                       the CTA then writes, per expert, each of its chunks'
+//                       first row within the CTA and the CTA's total;
+//   2. route_scan    -- one CTA turns the [CTA][expert] totals into the base
+//                       row of every (CTA, expert), the expert counts,
 //                       their exclusive prefix sum (group bounds), the
 //                       largest-first expert order, and the product kernels'
 //                       work list: every expert's rows cut into 128-row
@@ -34,30 +36,43 @@ route_hist_kernel(const int32_t* __restrict__ ids, int64_t n, int E, int nchunks
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x * kRouteWarps + warp;
   int32_t* h = sh + warp * E;
-  if (chunk >= nchunks) return;  // whole warp; no CTA barrier below
   for (int e = lane; e < E; e += 32) h[e] = 0;
   __syncwarp();
-  const int64_t beg = (int64_t)chunk * kRouteChunk;
-  const int64_t end = min(n, beg + kRouteChunk);
-  // all of this lane's ids first (independent loads), then the counts
-  int v[kRouteChunk / 32];
+  if (chunk < nchunks) {
+    const int64_t beg = (int64_t)chunk * kRouteChunk;
+    const int64_t end = min(n, beg + kRouteChunk);
+    // all of this lane's ids first (independent loads), then the counts
+    int v[kRouteChunk / 32];
 #pragma unroll
-  for (int j = 0; j < kRouteChunk / 32; j++) {
-    const int64_t i = beg + lane + 32 * j;
-    v[j] = i < end ? __ldg(ids + i) : 0;
-  }
-  bool bad = false;
+    for (int j = 0; j < kRouteChunk / 32; j++) {
+      const int64_t i = beg + lane + 32 * j;
+      v[j] = i < end ? __ldg(ids + i) : 0;
+    }
+    bool bad = false;
 #pragma unroll
-  for (int j = 0; j < kRouteChunk / 32; j++) {
-    if (beg + lane + 32 * j >= end) break;
-    if ((unsigned)v[j] < (unsigned)E)
-      atomicAdd(&h[v[j]], 1);
-    else
-      bad = true;
+    for (int j = 0; j < kRouteChunk / 32; j++) {
+      if (beg + lane + 32 * j >= end) break;
+      if ((unsigned)v[j] < (unsigned)E)
+        atomicAdd(&h[v[j]], 1);
+      else
+        bad = true;
+    }
+    if (bad) atomicOr(status, MOE_STATUS_BAD_EXPERT_ID);
   }
-  if (bad) atomicOr(status, MOE_STATUS_BAD_EXPERT_ID);
-  __syncwarp();
-  for (int e = lane; e < E; e += 32) hist[(int64_t)chunk * E + e] = h[e];
+  __syncthreads();
+  // per expert, the CTA's chunks in order: each chunk's first row within the
+  // CTA (hist rows 0 .. nchunks-1) and the CTA's total (row nchunks + CTA)
+  for (int e = threadIdx.x; e < E; e += kRouteWarps * 32) {
+    int run = 0;
+#pragma unroll
+    for (int w = 0; w < kRouteWarps; w++) {
+      const int c = blockIdx.x * kRouteWarps + w;
+      const int v = sh[w * E + e];
+      if (c < nchunks) hist[(int64_t)c * E + e] = run;
+      run += v;
+    }
+    hist[(int64_t)(nchunks + blockIdx.x) * E + e] = run;
+  }
 }
 
 // Exclusive prefix sum over the 1024 threads of the CTA (one value each).
@@ -161,7 +176,9 @@ __device__ __forceinline__ int expert_lists(int run, int E, int32_t* __restrict_
   return excl;
 }
 
-// One CTA of 1024 threads; thread e owns expert e (E <= 1024).
+// One CTA of 1024 threads; thread e owns expert e (E <= 1024).  It walks the
+// per-CTA totals (hist rows nchunks ..), not the chunks: each becomes the
+// expert's first routed row for that CTA's chunks.
 __global__ void __launch_bounds__(1024)
 route_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E,
                   int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
@@ -169,20 +186,22 @@ route_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E,
                   int32_t* __restrict__ ntiles) {
   __shared__ ScanShared sh;
   const int tid = threadIdx.x;
+  const int nctas = (nchunks + kRouteWarps - 1) / kRouteWarps;
+  int32_t* ctot = hist + (int64_t)nchunks * E;
   int run = 0;
   if (tid < E) {
 #pragma unroll 8
-    for (int c = 0; c < nchunks; c++) {
-      const int64_t idx = (int64_t)c * E + tid;
-      const int v = hist[idx];
-      hist[idx] = run;  // rows of expert tid in chunks before c
+    for (int b = 0; b < nctas; b++) {
+      const int64_t idx = (int64_t)b * E + tid;
+      const int v = ctot[idx];
+      ctot[idx] = run;  // rows of expert tid in CTAs before b
       run += v;
     }
   }
   const int excl = expert_lists(run, E, counts, offsets, order, tiles, ntiles, sh);
   if (tid < E) {
 #pragma unroll 8
-    for (int c = 0; c < nchunks; c++) hist[(int64_t)c * E + tid] += excl;
+    for (int b = 0; b < nctas; b++) ctot[(int64_t)b * E + tid] += excl;
   }
 }
 
@@ -290,7 +309,8 @@ route_scatter_kernel(const int32_t* __restrict__ ids, int64_t n, int E, int nchu
   const int chunk = blockIdx.x * kRouteWarps + warp;
   int32_t* h = sh + warp * E;
   if (chunk >= nchunks) return;
-  for (int e = lane; e < E; e += 32) h[e] = hist[(int64_t)chunk * E + e];
+  const int32_t* cbase = hist + (int64_t)(nchunks + blockIdx.x) * E;  // this CTA's chunks
+  for (int e = lane; e < E; e += 32) h[e] = hist[(int64_t)chunk * E + e] + cbase[e];
   __syncwarp();
   const int64_t beg = (int64_t)chunk * kRouteChunk;
   scatter_range(ids, beg, min(n, beg + kRouteChunk), E, h, row_src, dst_of);
@@ -367,7 +387,7 @@ NoAllocLayout noalloc_layout(int64_t n, int E) {
   L.order = 64;
   L.tiles = (L.order + E + 3) & ~(int64_t)3;  // 16-byte aligned
   L.hist = L.tiles + 4 * max_tiles(n, E);
-  L.total = L.hist + (int64_t)route_chunks(n) * E;
+  L.total = L.hist + route_hist_rows(n) * E;
   return L;
 }
 
