@@ -469,13 +469,16 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
         if ((b & 3) == 0 &&
             !(alive = mbar_wait(&dfull[de], (gd / kDxRing) & 1, s_abort, kTimeoutNs, false)))
           break;
+        // the block's activation scale, read before the wait for its product:
+        // under the MMAs' operand traffic a shared-memory read takes hundreds
+        // of cycles, and here it runs under that wait
+        const float dx = dxrow[de * (kTM * kScaleBox) + (b & 3)];
         if (!kFold && !(alive = mbar_wait(&wfull[gb % kDwRing], (gb / kDwRing) & 1, s_abort,
                                           kTimeoutNs, false)))
           break;
         if (!(alive = mbar_wait(&tfull[buf], (gb >> 1) & 1, s_abort, kTimeoutNs, false))) break;
         tc_fence_after();
         if (active) {
-          const float dx = dxrow[de * (kTM * kScaleBox) + (b & 3)];
           const float2 dx2 = make_float2(dx, dx);
 #pragma unroll
           for (int c = 0; c < 4; c++) {
