@@ -437,6 +437,10 @@ def other_config_line(M, cfg: int, steps: int, warmup: int, dev: str, stream,
         return {"workload": L.name, "error": "device status bits set"}
     t = time_stages(calls, steps, stream)
     ms = t["ms"] / steps
+    # the single-call layer replayed from one CUDA graph (no launch gaps)
+    dl.layer()
+    torch.cuda.synchronize()
+    graph = graph_leg(M, lambda: dl.layer(), dl.out, dl.out.clone(), steps, 1, s.T)
     hbm = layer_bytes(L)
     hbm_gbs = hbm["total"] / (ms * 1e-3) / 1e9
     prod = product_rooflines(s, t["mean"], peak)
@@ -452,7 +456,7 @@ def other_config_line(M, cfg: int, steps: int, warmup: int, dev: str, stream,
                              "unit": "GB/s", "frac": hbm_gbs / peaks["hbm"],
                              "algorithmic_bytes": hbm["total"],
                              "weights_bytes": hbm["weights"]},
-            "l2": l2_note(hbm)}
+            "l2": l2_note(hbm), "graph": graph}
     line["binding"] = ("hbm" if line["roofline_hbm"]["frac"] >
                        line["roofline_tensor"]["frac"] else "tensor")
     del dl
