@@ -221,10 +221,9 @@ SideStream* side_stream(cudaStream_t st) {
 
 // The status word starts every layer (and every moe_route) at zero.
 int run_route(Ctx& c, const int32_t* ids, cudaStream_t st) {
-  if (cudaMemsetAsync(c.v.status, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_LAUNCH;
   return launch_rc(launch_route(ids, rows_max(c.d), c.d.E, (int32_t*)(c.ws + c.L.hist),
                                 c.v.counts, c.v.offsets, c.v.order, c.v.row_src, c.v.dst_of,
-                                (int4*)(c.ws + c.L.tiles), c.v.status + 1, c.v.status, st));
+                                (int4*)(c.ws + c.L.tiles), c.v.status + 1, c.v.status, true, st));
 }
 
 int run_quant(Ctx& c, const float* x, cudaStream_t st) {

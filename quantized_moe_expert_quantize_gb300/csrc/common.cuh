@@ -69,10 +69,12 @@ __host__ __device__ inline int64_t max_tiles(int64_t rows, int E) {
 // tiles: int4 {expert, first routed row, rows, 0} [max_tiles]; ntiles: int32
 // [2] = {all tiles, tcgen05 tiles}.  The tcgen05 tiles come first, experts in
 // largest-first order; the small-row tiles are the tail [ntiles[1], ntiles[0]).
+// zero_status: the status word starts at zero (inside the one-launch routing,
+// a memset before the multi-launch one).
 cudaError_t launch_route(const int32_t* ids, int64_t n, int E, int32_t* hist,
                          int32_t* counts, int32_t* offsets, int32_t* order,
                          int32_t* row_src, int32_t* dst_of, int4* tiles, int32_t* ntiles,
-                         int32_t* status, cudaStream_t st);
+                         int32_t* status, bool zero_status, cudaStream_t st);
 
 // ---------------------------------------------------- elementwise kernels
 // q8 of x [T x K], scattered to routed rows: q [rows_max x K],

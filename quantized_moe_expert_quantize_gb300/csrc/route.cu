@@ -254,15 +254,17 @@ route_fused_kernel(const int32_t* __restrict__ ids, int64_t n, int E,
                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                    int32_t* __restrict__ order, int4* __restrict__ tiles,
                    int32_t* __restrict__ ntiles, int32_t* __restrict__ row_src,
-                   int32_t* __restrict__ dst_of, int32_t* __restrict__ status) {
+                   int32_t* __restrict__ dst_of, int32_t* __restrict__ status,
+                   int zero_status) {
   extern __shared__ int32_t hw[];  // [kFusedWarps][E]
   __shared__ ScanShared sh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (zero_status && tid == 0) *status = 0;  // before any bit below is set
   const int64_t S = ((n + kFusedWarps - 1) / kFusedWarps + 31) & ~(int64_t)31;
   const int64_t beg = min(n, (int64_t)warp * S), end = min(n, beg + S);
   int32_t* h = hw + warp * E;
   for (int e = lane; e < E; e += 32) h[e] = 0;
-  __syncwarp();
+  __syncthreads();  // (orders the status reset above before any atomicOr)
   bool bad = false;
   for (int64_t b0 = beg; b0 < end; b0 += 32 * 8) {
     int v[8];
@@ -321,7 +323,7 @@ route_scatter_kernel(const int32_t* __restrict__ ids, int64_t n, int E, int nchu
 cudaError_t launch_route(const int32_t* ids, int64_t n, int E, int32_t* hist,
                          int32_t* counts, int32_t* offsets, int32_t* order,
                          int32_t* row_src, int32_t* dst_of, int4* tiles, int32_t* ntiles,
-                         int32_t* status, cudaStream_t st) {
+                         int32_t* status, bool zero_status, cudaStream_t st) {
   if (n <= kFusedMaxEntries) {
     // one launch; its per-warp counts take 32*E int32 of shared memory
     const size_t fsmem = sizeof(int32_t) * kFusedWarps * E;
@@ -338,9 +340,13 @@ cudaError_t launch_route(const int32_t* ids, int64_t n, int E, int32_t* hist,
       ready[dev].store(ctx, std::memory_order_release);
     }
     route_fused_kernel<<<1, 1024, fsmem, st>>>(ids, n, E, counts, offsets, order, tiles, ntiles,
-                                               row_src, dst_of, status);
+                                               row_src, dst_of, status, zero_status ? 1 : 0);
     count_launch();
     return cudaGetLastError();
+  }
+  if (zero_status) {
+    const cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+    if (e != cudaSuccess) return e;
   }
   const int nchunks = route_chunks(n);
   const int grid = (nchunks + kRouteWarps - 1) / kRouteWarps;
@@ -436,6 +442,6 @@ extern "C" int moe_route_noalloc(const MoeLayerDesc* desc, const int32_t* topk_i
   const cudaError_t e =
       launch_route(topk_ids, n, desc->E, scratch + L.hist, counts, offsets, scratch + L.order,
                    row_src, dst_of, reinterpret_cast<int4*>(scratch + L.tiles), scratch + 1,
-                   scratch, st);
+                   scratch, false, st);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
