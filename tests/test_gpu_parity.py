@@ -458,15 +458,19 @@ def test_expert_row_counts_0_1_65(M):
     assert dl.get("counts").tolist() == [0, 1, 64, 65, 0, 129]
 
 
-SPLIT_COUNTS = [0, 1, 2, 7, 8, 9, 16, 17, 24, 25, 31, 32, 33, 64, 128, 160, 161, 300]
+SPLIT_COUNTS = [0, 1, 2, 3, 4, 5, 7, 8, 9, 16, 17, 24, 25, 31, 32, 33, 64, 128, 129, 132, 160,
+                161, 300]
 
 
-@pytest.mark.parametrize("fmts", [(synth.W2, synth.W2), (synth.W4NL, synth.Q8_0)])
+@pytest.mark.parametrize("fmts", [(synth.W2, synth.W2), (synth.W2, synth.W2, synth.GU_INTERLEAVED),
+                                  (synth.W4NL, synth.Q8_0)])
 def test_tile_split_row_counts(M, fmts):
-    """Row counts around every tile rule: small-row tiles of 1 to 4 n8
-    fragments (1..32 rows), the 32/33-row cutoff, a full 128-row tile alone,
-    with a 32-row small remainder (160), with a 33-row tcgen05 remainder
-    (161), and 2 full tiles + 44 (300)."""
+    """Row counts around every tile rule: W2 tiles of 1 to 4 rows (the dp4a
+    path, alone and as the remainder of a full tile: 129, 132), small-row
+    tiles of 1 to 4 n8 fragments (5..32 rows), the 32/33-row cutoff, a full
+    128-row tile alone, with a 32-row small remainder (160), with a 33-row
+    tcgen05 remainder (161), and 2 full tiles + 44 (300); in the layer, in
+    stages (GU in both gate/up layouts) and with the combine fused."""
     k, E = 1, len(SPLIT_COUNTS)
     ids = np.concatenate([np.full(c, e, np.int64) for e, c in enumerate(SPLIT_COUNTS)])
     ids = np.random.default_rng(1).permutation(ids)
