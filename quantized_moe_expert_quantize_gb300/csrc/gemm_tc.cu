@@ -596,19 +596,27 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
           nbc = min(kCB, a.bpr - (s / kSpc) * kCB);
         }
         const int st = it % kStages;
-        if (!(alive = mbar_wait(&empty[st], ((it / kStages) & 1) ^ 1, s_abort, kTimeoutNs))) break;
-        uint8_t* tileB = sB + st * kBBytes;
         const uint8_t* codes = raw;
         const uint16_t* scales = reinterpret_cast<const uint16_t*>(raw + nbc * I.NW * kCode);
+        // W2: this thread's two rows' codes and scales, read before the wait
+        // for the stage (the raw slot is already full; the reads run under it)
+        uint4 wc[2];
+        uint16_t wd[2];
+        if (kFold) {
+#pragma unroll
+          for (int rr = 0; rr < 2; rr++) {
+            const int idx = sc * I.NW + min(t + 128 * rr, I.NW - 1);
+            wc[rr] = *reinterpret_cast<const uint4*>(codes + idx * 16);
+            wd[rr] = scales[idx];
+          }
+        }
+        if (!(alive = mbar_wait(&empty[st], ((it / kStages) & 1) ^ 1, s_abort, kTimeoutNs))) break;
+        uint8_t* tileB = sB + st * kBBytes;
         if (kFold) {
 #pragma unroll
           for (int rr = 0; rr < 2; rr++) {
             const int r = t + 128 * rr;
-            if (r < I.NW) {
-              const int idx = sc * I.NW + r;
-              decode_w2_store(*reinterpret_cast<const uint4*>(codes + idx * 16), scales[idx],
-                              tileB, r);
-            }
+            if (r < I.NW) decode_w2_store(wc[rr], wd[rr], tileB, r);
           }
         } else {
           // two blocks per stage, each with its own scale slot in the ring
