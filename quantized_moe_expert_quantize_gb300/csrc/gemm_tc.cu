@@ -445,9 +445,13 @@ gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmap,
     uint32_t gb = 0;  // 32-value blocks consumed so far (TMEM buffer gb & 1)
     uint32_t gd = 0;  // activation-scale entries consumed so far
     bool alive = true;
+    // the next item's tile entry is loaded one item ahead (its global-memory
+    // latency then runs under the current item)
+    int4 tnext = load_tile(a, blockIdx.x, total, n_wtiles);
     for (int item = blockIdx.x; item < (int)total && alive; item += (int)stride) {
       const int wtile = item % n_wtiles;
-      const Item I = make_item<FMT>(a, s_eoff, load_tile(a, item, total, n_wtiles), wtile);
+      const Item I = make_item<FMT>(a, s_eoff, tnext, wtile);
+      tnext = load_tile(a, item + stride, total, n_wtiles);
       if (!I.ok) {
         if (lane == 0 && warp == 0) atomicOr(a.status, MOE_STATUS_BAD_OFFSET);
         continue;
