@@ -388,6 +388,12 @@ __device__ __forceinline__ bool item_dp4a(const SmArgs& a, const uint8_t* smem, 
     const uint32_t buf = dc & 1;
     const uint32_t words = conv_s + buf * (kDp4aRows * 64 * 4);  // [row][64]
     const uint32_t sums = csum_s + buf * (kDp4aRows * 8 * 4);    // [row][8]
+    // this thread's first code words and scale, read now: they run under the
+    // conversion and its wait (the next block's are read under each block)
+    uint32_t cj = sp + (uint32_t)(tid * kCode);                             // codes of (block j, row tid)
+    uint32_t sj = sp + (uint32_t)(nbc * nw * kCode) + (uint32_t)(tid * 2);  // its fp16 scale
+    uint4 w4 = lds128(cj);
+    float dw = lds_half_as_f32(sj);
     // ---- the chunk's activation words: thread tid < 64U makes word tid
     // (row tid/64, group G, shift s) from stored words 8G+s (values s, s+8)
     // and 8G+s+4 (values s+4, s+12); 1536 + q in fp16 has q's two's
@@ -419,18 +425,21 @@ __device__ __forceinline__ bool item_dp4a(const SmArgs& a, const uint8_t* smem, 
     }
     // ---- this thread's row against the U rows
     const uint32_t dxs = sp + kRawBytes + kActBytes;  // [32 rows][8] fp32 (this chunk's 8 blocks)
-    uint32_t cj = sp + (uint32_t)(tid * kCode);                       // codes of (block j, row tid)
-    uint32_t sj = sp + (uint32_t)(nbc * nw * kCode) + (uint32_t)(tid * 2);  // its fp16 scale
 #pragma unroll 1
-    for (int j = 0; j < nbc; j++, cj += nw * kCode, sj += nw * 2) {
-      const uint4 w4 = lds128(cj);
-      const float dw = lds_half_as_f32(sj);
+    for (int j = 0; j < nbc; j++) {
       const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};  // groups 4j .. 4j+3
       uint32_t cw[4][4];                                 // [group][shift]: codes as bytes
 #pragma unroll
       for (int g = 0; g < 4; g++)
 #pragma unroll
         for (int sh = 0; sh < 4; sh++) cw[g][sh] = (wv[g] >> (2 * sh)) & 0x03030303u;
+      const float dwj = dw;
+      if (j + 1 < nbc) {
+        cj += nw * kCode;
+        sj += nw * 2;
+        w4 = lds128(cj);
+        dw = lds_half_as_f32(sj);
+      }
 #pragma unroll
       for (int r = 0; r < U; r++) {
         int isum[2] = {0, 0};  // q8 blocks 2j, 2j+1
@@ -447,7 +456,7 @@ __device__ __forceinline__ bool item_dp4a(const SmArgs& a, const uint8_t* smem, 
           const int qb = 2 * j + qq;
           const int qs = (int)lds32(sums + (uint32_t)(r * 32 + qb * 4));
           const float dx = lds_f32(dxs + (uint32_t)((r * kDxW + qb) * 4));
-          acc[r] = __fmaf_rn(dx, __fmul_rn(dw, (float)(isum[qq] - 2 * qs)), acc[r]);
+          acc[r] = __fmaf_rn(dx, __fmul_rn(dwj, (float)(isum[qq] - 2 * qs)), acc[r]);
         }
       }
     }
