@@ -654,6 +654,37 @@ def test_host_buffers_entry_point(M):
     M.moe_prefill_layer_host(dl.desc, hx, hi, hw, dl.pack, dl.eoff, ho, io, dl.ws)
     torch.cuda.synchronize()
     assert np.array_equal(ho.numpy(), ref)
+    # two calls enqueued back to back on one staging buffer: the second
+    # call's x (copied on the copy stream) must wait for the first call's q8
+    # step
+    ho2 = torch.empty_like(ho)
+    hx2 = hx.clone()
+    hx2.mul_(-1.0)
+    M.moe_prefill_layer_host(dl.desc, hx2, hi, hw, dl.pack, dl.eoff, ho2, io, dl.ws)
+    M.moe_prefill_layer_host(dl.desc, hx, hi, hw, dl.pack, dl.eoff, ho, io, dl.ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(ho.numpy(), ref)
+    dl.x.copy_(hx2.cuda())
+    dl.run_layer()
+    assert np.array_equal(ho2.numpy(), dl.out.cpu().numpy())
+
+
+def test_host_buffers_fewer_tokens_than_chunks(M):
+    """The host-buffer layer at T = 5 (some token chunks of its combine and
+    out copy are empty) equals the device entry."""
+    s = synth.LayerShape(5, 256, 64, 8, 2, synth.W2, synth.W2)
+    L = synth.make_layer(s, seed=21)
+    dl = DeviceLayer(M, L)
+    dl.run_layer()
+    ref = dl.out.cpu().numpy()
+    hx = torch.from_numpy(L.x).pin_memory()
+    hi = torch.from_numpy(L.topk_ids).pin_memory()
+    hw = torch.from_numpy(L.topk_w).pin_memory()
+    ho = torch.empty((s.T, s.d), dtype=torch.float32).pin_memory()
+    io = torch.empty(M.host_io_bytes(dl.desc), dtype=torch.uint8, device="cuda")
+    M.moe_prefill_layer_host(dl.desc, hx, hi, hw, dl.pack, dl.eoff, ho, io, dl.ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(ho.numpy(), ref)
 
 
 def test_repeat_is_deterministic(M):
