@@ -68,7 +68,8 @@ constexpr int kDxBytes = kRows * (kChunkVals / 32) * 4;  // 1,024: 32 rows x 8 s
 // slots 1024-byte aligned: the activation boxes use the 128-byte swizzle
 constexpr int kSlotBytes = (kRawBytes + kActBytes + kDxBytes + 1023) & ~1023;
 constexpr int kActBox = 64;                                  // values per activation box (128 B)
-constexpr int kOffBar = kSlots * kSlotBytes;
+constexpr int kOffBar = kSlots * kSlotBytes;  // full[kSlots] mbarriers
+constexpr int kOffRel = kOffBar + kSlots * 8;  // per slot: warps done with it (int, 8 B apart)
 constexpr int kOffMisc = kOffBar + 2 * kSlots * 8;
 // misc: abort flag (+0), W4NL table (+64), warp-pair barriers [2][kWarps/2]
 // (+128), the ring producer's state (+192); then the warp-pair amax exchange
@@ -84,7 +85,10 @@ constexpr int kOffConv = kOffAmax + 2 * kWarps * kRows * 4;
 constexpr int kOffConvSum = kOffConv + 2 * kDp4aRows * 64 * 4;
 constexpr int kOffUp = kOffConvSum + 2 * kDp4aRows * 8 * 4;
 constexpr int kOffDbar = kOffUp + kDp4aRows * (kTN / 2) * 4;
-constexpr int kSmemBytes = kOffDbar + 64 + 1024;  // + alignment slack
+// per slot, written by the ring producer with the slot's item: {first routed
+// row, rows, weight tile, its rows}
+constexpr int kOffInfo = kOffDbar + 64;
+constexpr int kSmemBytes = kOffInfo + kSlots * 16 + 1024;  // + alignment slack
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 constexpr int kModeGU = 0, kModeSwiglu = 1, kModeDown = 2;
 static_assert(kSlotBytes % 1024 == 0 && kRawBytes % 1024 == 0, "swizzled boxes 1024-byte aligned");
@@ -207,7 +211,7 @@ __device__ __forceinline__ float lds_half_as_f32(uint32_t a) {
 // stored.  Every shared-memory address is a per-lane offset, fixed for the
 // item, plus a per-chunk base advanced once a block.
 template <int FMT, int NNT, typename Refill>
-__device__ __forceinline__ bool consume_item(const uint8_t* smem, uint64_t* full, uint64_t* empty,
+__device__ __forceinline__ bool consume_item(const uint8_t* smem, uint64_t* full,
                                              volatile int* s_abort, uint32_t& cc, int nchunks,
                                              int bpr, int nw, const int (&rbase)[2],
                                              const uint16_t* s_lut, int lane,
@@ -322,8 +326,6 @@ __device__ __forceinline__ bool consume_item(const uint8_t* smem, uint64_t* full
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
     refill(cc);
   }
   return true;
@@ -365,7 +367,7 @@ __device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
 // bits equal the m16n8k16 path's.
 template <int MODE, int U, typename Refill>
 __device__ __forceinline__ bool item_dp4a(const SmArgs& a, const uint8_t* smem, uint64_t* full,
-                                          uint64_t* empty, uint64_t* cbar, uint64_t* ubar,
+                                          uint64_t* cbar, uint64_t* ubar,
                                           volatile int* s_abort, uint32_t& cc, uint32_t& dc,
                                           uint32_t& uc, int nchunks, int nw, int4 t, int wt,
                                           Refill&& refill) {
@@ -460,8 +462,6 @@ __device__ __forceinline__ bool item_dp4a(const SmArgs& a, const uint8_t* smem, 
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
     refill(cc);
   }
 
@@ -549,13 +549,15 @@ __device__ __forceinline__ ItemInfo item_info(const SmArgs& a, int first, int n_
 // drew cheap items draws more.  Items differ in cost several times over (an
 // m16n8k16 item of 17-32 rows against a dp4a item of one row), and with a
 // fixed round-robin deal the multiprocessors sat idle a fifth of the time
-// at 128 tokens.  The producer writes each chunk's item into s_item[slot]
-// before it arms the slot; after the list it arms one more slot with no
-// copies and item -1, which ends the consumers' loop.  routing zeroes the
-// counters, and the last CTA to finish zeroes them again for the next launch.
+// at 128 tokens.  The producer writes each chunk's item into s_item[slot],
+// and the item's rows and weight tile into the slot's info record, before it
+// arms the slot (the consumers take them from there, not from the work list
+// in global memory); after the list it arms one more slot with no copies and
+// item -1, which ends the consumers' loop.  routing zeroes the counters, and
+// the last CTA to finish zeroes them again for the next launch.
 //
-// The load side of the ring (lane 0 of warp 0): the next (item, chunk) to
-// load, in the order the warps consume them.  Per chunk: one bulk copy of
+// The load side of the ring (run by whichever warp releases a slot last):
+// the next (item, chunk) to load, in the order the warps consume them.  Per chunk: one bulk copy of
 // the raw weight chunk and the tile's activation rows and scales in 2-D TMA
 // boxes of 16 rows (rows past the tile land in rows that are never read).
 struct Producer {
@@ -564,6 +566,7 @@ struct Producer {
   int row0, nw, nbox;
   uint32_t issued;
   int ended;    // the closing slot is armed
+  int rows, wt;  // the item's routed rows and weight tile
 };
 __device__ __forceinline__ void prod_seek(Producer& p, const SmArgs& a, int first, int total,
                                           int n_wtiles, int64_t mbytes) {
@@ -581,6 +584,8 @@ __device__ __forceinline__ void prod_seek(Producer& p, const SmArgs& a, int firs
     p.c = 0;
     p.row0 = I.t.y;
     p.nw = I.nw;
+    p.rows = I.t.z;
+    p.wt = I.wt;
     p.nbox = I.t.z > kBoxRows ? 2 : 1;
     p.wbase = a.pack + I.off + (int64_t)I.wt * kTN * a.bpr * a.bb;
     return;
@@ -604,6 +609,9 @@ __device__ __forceinline__ void prod_issue(Producer& p, uint8_t* smem, uint64_t*
     p.issued++;
     return;
   }
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(smem) + kOffInfo + 16 * slot),
+               "r"(p.row0), "r"(p.rows), "r"(p.wt), "r"(p.nw)
+               : "memory");
   s_item[slot] = p.item;
   uint8_t* sp = smem + slot * kSlotBytes;
   const int nbc = min(kCB, a.bpr - p.c * kCB);
@@ -635,7 +643,7 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
   // round trip would hide the shared address space from the compiler)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* empty = full + kSlots;
+  int* s_rel = reinterpret_cast<int*>(smem + kOffRel);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc);
   uint16_t* s_lut = reinterpret_cast<uint16_t*>(smem + kOffMisc + 64);
   uint64_t* pairbar = reinterpret_cast<uint64_t*>(smem + kOffMisc + 128);
@@ -646,7 +654,7 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
   if (tid == 0) {
     for (int i = 0; i < kSlots; i++) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kWarps);
+      s_rel[2 * i] = 0;
     }
     for (int i = 0; i < kWarps; i++) mbar_init(&pairbar[i], 64);  // both warps of a pair
     for (int i = 0; i < 3; i++) mbar_init(&cbar[i], kWarps);      // lane 0 of every warp
@@ -663,10 +671,11 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
   const int nchunks = (a.bpr + chunk_blocks(FMT) - 1) / chunk_blocks(FMT);
   const int64_t mbytes = (int64_t)a.N_out * a.bpr * a.bb;
 
-  // ring: prefill every slot, then lane 0 of warp 0 refills a slot as soon
-  // as all warps have released it
-  // (its state lives in shared memory: only thread 0 touches it, and as
-  // registers it would be held by every thread of the CTA)
+  // ring: thread 0 prefills every slot; then lane 0 of the last warp to
+  // release a slot refills it, so no warp waits for the others to finish a
+  // chunk (with warp 0 waiting on a release barrier instead, 128 tokens took
+  // 2 % longer).  The producer state lives in shared memory: one thread at a
+  // time touches it, and as registers it would be held by every thread.
   Producer& prod = *reinterpret_cast<Producer*>(smem + kOffMisc + 192);
   volatile int* s_item = reinterpret_cast<volatile int*>(smem + kOffMisc + 240);
   if (tid == 0) {
@@ -679,15 +688,23 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
       prod_issue<FMT>(prod, smem, full, a, &tmap, &tmap_d, first, total, n_wtiles, mbytes, nchunks);
   }
   auto refill = [&](uint32_t done) {  // chunk `done` was consumed by this warp
-    if (warp == 0) {
-      if (lane == 0 && !prod.ended) {
-        // all warps released chunk `done`'s slot: load the chunk kSlots ahead
-        if (mbar_wait(&empty[done % kSlots], (done / kSlots) & 1, s_abort, kTimeoutNs, false))
+    __syncwarp();
+    if (lane == 0) {
+      // the last warp to release chunk `done`'s slot loads the chunk kSlots
+      // ahead into it; the chunks are released in order, so the loads are
+      // issued in order, one at a time
+      int* rel = s_rel + 2 * (done % kSlots);
+      __threadfence_block();
+      if (atomicAdd(rel, 1) == kWarps - 1) {
+        *rel = 0;
+        __threadfence_block();
+        if (!*reinterpret_cast<volatile int*>(&prod.ended))
           prod_issue<FMT>(prod, smem, full, a, &tmap, &tmap_d, first, total, n_wtiles, mbytes,
                           nchunks);
+        __threadfence_block();
       }
-      __syncwarp();
     }
+    __syncwarp();
   };
 
   const int g = lane >> 2, cq = lane & 3;
@@ -702,13 +719,14 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
       break;
     const int item = s_item[cc % kSlots];
     if (item < 0) break;  // the closing slot
-    const ItemInfo I = item_info(a, first, n_wtiles, mbytes, item);
-    const int4 t = I.t;
-    const int wt = I.wt, nw = I.nw;
+    // the item's rows and weight tile, as the producer found them
+    const uint4 inf = lds128(smem_u32(smem) + kOffInfo + 16 * (cc % kSlots));
+    const int4 t = make_int4(0, (int)inf.x, (int)inf.y, 0);
+    const int wt = (int)inf.z, nw = (int)inf.w;
     if constexpr (kW2) {
       if (t.z <= kDp4aRows) {
 #define MOE_SMALL_DP4A(N)                                                                       \
-  item_dp4a<MODE, N>(a, smem, full, empty, cbar, cbar + 2, s_abort, cc, dc, uc, nchunks, nw, t, wt, \
+  item_dp4a<MODE, N>(a, smem, full, cbar, cbar + 2, s_abort, cc, dc, uc, nchunks, nw, t, wt, \
                      refill)
         alive = t.z == 1   ? MOE_SMALL_DP4A(1)
                 : t.z == 2 ? MOE_SMALL_DP4A(2)
@@ -736,7 +754,7 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
 #pragma unroll
           for (int i = 0; i < 4; i++) acc[mt][nt][i] = 0.0f;
 #define MOE_SMALL_CONSUME(N)                                                                  \
-  consume_item<FMT, N>(smem, full, empty, s_abort, cc, nchunks, a.bpr, nw, rbase, s_lut, lane, \
+  consume_item<FMT, N>(smem, full, s_abort, cc, nchunks, a.bpr, nw, rbase, s_lut, lane, \
                        acc, refill)
       alive = nnt == 1   ? MOE_SMALL_CONSUME(1)
               : nnt == 2 ? MOE_SMALL_CONSUME(2)
@@ -853,7 +871,9 @@ gemm_small_kernel(const SmArgs a, const __grid_constant__ CUtensorMap tmap,
       }
     }
   }
-  // copies still in flight after an abort land before the CTA exits
+  // copies still in flight after an abort land before the CTA exits (every
+  // warp has issued its last load)
+  __syncthreads();
   if (tid == 0)
     for (uint32_t i = cc; i < prod.issued; i++)
       if (!mbar_wait(&full[i % kSlots], (i / kSlots) & 1, s_abort, kTimeoutNs, false)) break;
