@@ -88,8 +88,17 @@ enum { MOE_GU_SPLIT = 0, MOE_GU_INTERLEAVED = 1 };
  *     moe_combine, so out is bit-identical either way ("Strata #3752",
  *     Validation: the prompt path's combine fused with the write).  Dm is
  *     still written (a row cannot know it is the last before it has
- *     published its values). */
-enum { MOE_FLAG_FUSED_COMBINE = 1 };
+ *     published its values).
+ *   MOE_FLAG_HOST_OUT_DEFERRED  moe_prefill_layer_host does not make `stream`
+ *     wait for out's copy back to the host: in a run of calls, one call's
+ *     out goes back while the next call computes.  Every out copied by the
+ *     host-buffer calls so far is complete once moe_host_out_join(stream)
+ *     has been enqueued and `stream` has been synchronised.  Each call's
+ *     combine waits for the previous call's copy before it writes the
+ *     staging buffer.  Under stream capture, and with MOE_FLAG_FUSED_COMBINE,
+ *     out's copy runs on `stream` and the flag changes nothing.  Other entry
+ *     points ignore it. */
+enum { MOE_FLAG_FUSED_COMBINE = 1, MOE_FLAG_HOST_OUT_DEFERRED = 2 };
 
 enum {
   MOE_OK = 0,
@@ -246,9 +255,14 @@ int moe_prefill_layer(const MoeLayerDesc *desc, const float *x,
  * `io` has quantised its x (so a call enqueued while the previous one
  * computes brings its x in meanwhile), and out leaves in token chunks on a
  * second copy stream right behind the combine; `stream` waits for the last
- * chunk.  Calls whose work overlaps on the same `io` (other streams, other
- * threads) race, as on one workspace.  Under stream capture all copies run
- * on `stream` in order. */
+ * chunk (unless desc->flags has MOE_FLAG_HOST_OUT_DEFERRED).  Calls whose
+ * work overlaps on the same `io` (other streams, other threads) race, as on
+ * one workspace.  Under stream capture all copies run on `stream` in order.
+ *
+ * moe_host_out_join makes `stream` wait for every out copy that host-buffer
+ * calls on the current device have enqueued so far (MOE_OK and nothing
+ * enqueued when there is none); with MOE_FLAG_HOST_OUT_DEFERRED the caller
+ * enqueues it, then synchronises `stream`, before reading any h_out. */
 size_t moe_host_io_bytes(const MoeLayerDesc *desc);
 int moe_prefill_layer_host(const MoeLayerDesc *desc, const float *h_x,
                            const int32_t *h_topk_ids, const float *h_topk_w,
@@ -256,6 +270,7 @@ int moe_prefill_layer_host(const MoeLayerDesc *desc, const float *h_x,
                            const int64_t *expert_offsets, float *h_out,
                            void *io, size_t io_bytes, void *workspace,
                            size_t workspace_bytes, moe_stream_t stream);
+int moe_host_out_join(moe_stream_t stream);
 
 /* Stage entry points (tests and profiling).  Each runs one step of the
  * layer, reading and writing the workspace regions of MoeWorkspaceView, in

@@ -22,6 +22,7 @@ MOE_FMT_Q8_0 = 3
 MOE_GU_SPLIT = 0
 MOE_GU_INTERLEAVED = 1
 MOE_FLAG_FUSED_COMBINE = 1
+MOE_FLAG_HOST_OUT_DEFERRED = 2
 
 MOE_OK = 0
 MOE_ERR_NULL = -1
@@ -42,7 +43,7 @@ MOE_STATUS_BAD_ROUTING = 8
 # every symbol include/moe_prefill.h declares
 EXPORTS = (
     "moe_prefill_workspace_bytes", "moe_workspace_view", "moe_prefill_layer",
-    "moe_host_io_bytes", "moe_prefill_layer_host", "moe_route", "moe_quant_q8",
+    "moe_host_io_bytes", "moe_prefill_layer_host", "moe_host_out_join", "moe_route", "moe_quant_q8",
     "moe_gate_up", "moe_swiglu_quant", "moe_down", "moe_down_combine", "moe_combine",
     "moe_read_status",
     "moe_check_device", "moe_status_string", "moe_kernel_launches", "moe_route_noalloc",
@@ -99,6 +100,8 @@ def lib(build_if_missing: bool = False) -> ctypes.CDLL:
         L.moe_host_io_bytes.restype = sz
         L.moe_prefill_layer_host.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, sz, vp, sz, vp]
         L.moe_prefill_layer_host.restype = i32
+        L.moe_host_out_join.argtypes = [vp]
+        L.moe_host_out_join.restype = i32
         L.moe_route.argtypes = [dp, vp, vp, sz, vp]
         L.moe_route.restype = i32
         L.moe_quant_q8.argtypes = [dp, vp, vp, sz, vp]
@@ -260,6 +263,10 @@ def moe_prefill_layer_host(desc, h_x, h_topk_ids, h_topk_w, weight_pack, expert_
         _ptr(h_out, torch.float32, device=False), _ptr(io, torch.uint8), io.numel(),
         _ptr(workspace, torch.uint8), workspace.numel(), _stream(stream)),
         "moe_prefill_layer_host")
+
+
+def moe_host_out_join(stream=None):
+    _check(lib().moe_host_out_join(_stream(stream)), "moe_host_out_join")
 
 
 def moe_route(desc, topk_ids, workspace, stream=None):

@@ -111,7 +111,7 @@ int validate_desc(const MoeLayerDesc* d) {
   auto fmt_ok = [](int f) { return f == MOE_FMT_W2 || f == MOE_FMT_W4NL || f == MOE_FMT_Q8_0; };
   if (!fmt_ok(d->gu_fmt) || !fmt_ok(d->down_fmt) ||
       (d->gu_layout != MOE_GU_SPLIT && d->gu_layout != MOE_GU_INTERLEAVED) ||
-      (d->flags & ~(uint32_t)MOE_FLAG_FUSED_COMBINE) != 0 ||
+      (d->flags & ~(uint32_t)(MOE_FLAG_FUSED_COMBINE | MOE_FLAG_HOST_OUT_DEFERRED)) != 0 ||
       d->reserved != 0)
     return MOE_ERR_FORMAT;
   if (d->weight_pack_bytes < 0) return MOE_ERR_SHAPE;
@@ -182,6 +182,7 @@ struct SideStream {
   cudaEvent_t x_in = nullptr, x_free = nullptr, comb = nullptr, out_done = nullptr,
               entry = nullptr;
   const void* last_io = nullptr;  // staging buffer x_free was last recorded for
+  bool out_pending = false;       // out_done has been recorded
   uint64_t ctx = 0;    // context the handles belong to
   bool tried = false;  // creation was attempted in that context
 };
@@ -492,7 +493,11 @@ size_t moe_host_io_bytes(const MoeLayerDesc* desc) {
 //  - the combine runs in token chunks, and each chunk's rows of out go back
 //    on a second copy stream as soon as they are written; the caller's
 //    stream then waits for the last chunk, so out is complete once `stream`
-//    is.
+//    is -- or, with MOE_FLAG_HOST_OUT_DEFERRED, it does not, and the copy
+//    runs on under the next call's products (out is then complete after
+//    moe_host_out_join).  The first combine chunk waits for the previous
+//    call's last out copy, so the staging buffer is not overwritten while it
+//    is still being read.
 // Under stream capture, or without the copy streams, every copy runs on the
 // caller's stream in order.
 constexpr int kOutChunks = 8;
@@ -562,6 +567,7 @@ int moe_prefill_layer_host(const MoeLayerDesc* desc, const float* h_x, const int
   }
   if ((rc = run_gemm(c, 1, weight_pack, expert_offsets, st))) return rc;
   lock.lock();
+  if (!ok(cudaStreamWaitEvent(st, sd->out_done, 0))) return MOE_ERR_LAUNCH;
   const size_t row_bytes = sizeof(float) * c.d.d;
   for (int ch = 0; ch < kOutChunks; ch++) {
     const int64_t t0 = (int64_t)(T * ch / kOutChunks), t1 = (int64_t)(T * (ch + 1) / kOutChunks);
@@ -574,10 +580,21 @@ int moe_prefill_layer_host(const MoeLayerDesc* desc, const float* h_x, const int
                             (t1 - t0) * row_bytes, cudaMemcpyDeviceToHost, sd->d2h)))
       return MOE_ERR_LAUNCH;
   }
-  if (!ok(cudaEventRecord(sd->out_done, sd->d2h)) ||
-      !ok(cudaStreamWaitEvent(st, sd->out_done, 0)))
+  if (!ok(cudaEventRecord(sd->out_done, sd->d2h))) return MOE_ERR_LAUNCH;
+  sd->out_pending = true;
+  if (!(c.d.flags & MOE_FLAG_HOST_OUT_DEFERRED) && !ok(cudaStreamWaitEvent(st, sd->out_done, 0)))
     return MOE_ERR_LAUNCH;
   return MOE_OK;
+}
+
+int moe_host_out_join(moe_stream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  const SideStream& sd = g_side[dev];
+  if (sd.ctx != current_context_id() || !sd.out_pending) return MOE_OK;
+  return cudaStreamWaitEvent((cudaStream_t)stream, sd.out_done, 0) == cudaSuccess ? MOE_OK
+                                                                                    : MOE_ERR_LAUNCH;
 }
 
 int moe_read_status(const MoeLayerDesc* desc, void* ws, size_t bytes, int32_t* status,

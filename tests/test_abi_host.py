@@ -55,7 +55,7 @@ def test_workspace_bytes_layout(lib):
     ("E", 0, M.MOE_ERR_SHAPE), ("E", 2048, M.MOE_ERR_SHAPE), ("k", 0, M.MOE_ERR_SHAPE),
     ("k", 9, M.MOE_ERR_SHAPE), ("T", -1, M.MOE_ERR_SHAPE), ("gu_fmt", 4, M.MOE_ERR_FORMAT),
     ("down_fmt", 0, M.MOE_ERR_FORMAT), ("gu_layout", 2, M.MOE_ERR_FORMAT),
-    ("flags", 2, M.MOE_ERR_FORMAT), ("flags", 3, M.MOE_ERR_FORMAT)])
+    ("flags", 4, M.MOE_ERR_FORMAT), ("flags", 7, M.MOE_ERR_FORMAT)])
 def test_bad_descriptor_rejected(lib, field, value, code):
     d = M.make_desc(64, 256, 64, 8, 2)
     setattr(d, field, value)
@@ -66,12 +66,17 @@ def test_bad_descriptor_rejected(lib, field, value, code):
     assert rc == code
 
 
-def test_fused_combine_flag_is_accepted(lib):
-    """MOE_FLAG_FUSED_COMBINE is the one known flag: the layer keeps its
-    workspace size (the fused combine's counters are always laid out)."""
+def test_layer_flags_are_accepted(lib):
+    """MOE_FLAG_FUSED_COMBINE and MOE_FLAG_HOST_OUT_DEFERRED are the known
+    flags: the layer keeps its workspace size (the fused combine's counters
+    are always laid out), and any other bit is refused."""
     d0 = M.make_desc(64, 256, 64, 8, 2)
-    d1 = M.make_desc(64, 256, 64, 8, 2, flags=M.MOE_FLAG_FUSED_COMBINE)
-    assert M.workspace_bytes(d1) == M.workspace_bytes(d0) > 0
+    for f in (M.MOE_FLAG_FUSED_COMBINE, M.MOE_FLAG_HOST_OUT_DEFERRED,
+              M.MOE_FLAG_FUSED_COMBINE | M.MOE_FLAG_HOST_OUT_DEFERRED):
+        d1 = M.make_desc(64, 256, 64, 8, 2, flags=f)
+        assert M.workspace_bytes(d1) == M.workspace_bytes(d0) > 0
+    bad = M.make_desc(64, 256, 64, 8, 2, flags=4)
+    assert lib.moe_prefill_workspace_bytes(ctypes.byref(bad)) == 0
 
 
 def _fake(addr):

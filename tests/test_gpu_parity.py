@@ -669,6 +669,35 @@ def test_host_buffers_entry_point(M):
     assert np.array_equal(ho2.numpy(), dl.out.cpu().numpy())
 
 
+def test_host_buffers_deferred_out(M):
+    """With MOE_FLAG_HOST_OUT_DEFERRED, three host-buffer calls enqueued back
+    to back on one staging buffer (each call's out copy left running under
+    the next call's products, the next combine waiting for it) give, after
+    moe_host_out_join and a synchronise, each call's device-entry result."""
+    L = SMALL["mid_w2_w2"]()
+    dl = DeviceLayer(M, L)
+    hi = torch.from_numpy(L.topk_ids).pin_memory()
+    hw = torch.from_numpy(L.topk_w).pin_memory()
+    xs = [torch.from_numpy(L.x).pin_memory()]
+    xs.append(xs[0].clone().mul_(-1.0))
+    xs.append(xs[0].clone().mul_(0.5))
+    refs = []
+    for hx in xs:
+        dl.x.copy_(hx.cuda())
+        dl.run_layer()
+        refs.append(dl.out.cpu().numpy().copy())
+    desc = type(dl.desc).from_buffer_copy(dl.desc)
+    desc.flags = M.MOE_FLAG_HOST_OUT_DEFERRED
+    io = torch.empty(M.host_io_bytes(desc), dtype=torch.uint8, device="cuda")
+    outs = [torch.full((L.shape.T, L.shape.d), float("nan")).pin_memory() for _ in xs]
+    for hx, ho in zip(xs, outs):
+        M.moe_prefill_layer_host(desc, hx, hi, hw, dl.pack, dl.eoff, ho, io, dl.ws)
+    M.moe_host_out_join()
+    torch.cuda.synchronize()
+    for ho, ref in zip(outs, refs):
+        assert np.array_equal(ho.numpy(), ref)
+
+
 def test_host_buffers_fewer_tokens_than_chunks(M):
     """The host-buffer layer at T = 5 (some token chunks of its combine and
     out copy are empty) equals the device entry."""
