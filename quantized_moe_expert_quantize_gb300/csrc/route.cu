@@ -106,7 +106,7 @@ __device__ __forceinline__ int block_excl_scan(int v, int32_t* s_warp) {
 // (returned: the expert's first routed row), the largest-first order and
 // the work list of tiles with its split count.
 struct ScanShared {
-  __align__(16) int32_t cnt[1024];  // rows of expert e (0 past E)
+  __align__(16) int32_t cnt[1024];  // rows of expert e (0 past E), or its rank key
   int32_t tiles[1024];              // tcgen05 tiles of the expert at rank r, then their first
   int32_t small[1024];              // small-row tiles of the expert at rank r, then their first
   int32_t warp[32];
@@ -118,7 +118,14 @@ __device__ __forceinline__ int expert_lists(int run, int E, int32_t* __restrict_
                                             int32_t* __restrict__ ntiles, ScanShared& sh) {
   const int tid = threadIdx.x;
   if (tid < E) counts[tid] = run;
-  sh.cnt[tid] = run;
+  // experts rank by (count descending, id ascending).  While every count
+  // fits in 22 bits the pair is one unsigned key, the count above 1023 - id,
+  // and an expert's rank is the number of larger keys (one compare and one
+  // add per expert instead of four tests: the ranking was most of the
+  // routing step's time)
+  const bool wide = __syncthreads_or(run >= (1 << 22));
+  const uint32_t key = ((uint32_t)run << 10) | (uint32_t)(1023 - tid);
+  sh.cnt[tid] = wide ? run : (int32_t)key;
   sh.tiles[tid] = 0;
   sh.small[tid] = 0;
   const int excl = block_excl_scan(run, sh.warp);  // also orders the writes above
@@ -132,14 +139,25 @@ __device__ __forceinline__ int expert_lists(int run, int E, int32_t* __restrict_
   if (tid < E) {
     offsets[tid] = excl;
     if (tid == E - 1) offsets[E] = excl + run;
-    // rank by (count descending, id ascending); cnt past E is 0 with ids
-    // above every expert's, so whole int4 reads count nothing extra
-    for (int e2 = 0; e2 < E; e2 += 4) {
-      const int4 c4 = *reinterpret_cast<const int4*>(sh.cnt + e2);
-      rank += (c4.x > run) || (c4.x == run && e2 < tid);
-      rank += (c4.y > run) || (c4.y == run && e2 + 1 < tid);
-      rank += (c4.z > run) || (c4.z == run && e2 + 2 < tid);
-      rank += (c4.w > run) || (c4.w == run && e2 + 3 < tid);
+    // past E the entries are those of count 0 with ids above every
+    // expert's, so whole 16-byte reads count nothing extra (E <= 1024)
+    if (!wide) {
+      int r0 = 0, r1 = 0;
+      for (int e2 = 0; e2 < E; e2 += 8) {
+        const uint4 a = *reinterpret_cast<const uint4*>(sh.cnt + e2);
+        const uint4 b = *reinterpret_cast<const uint4*>(sh.cnt + e2 + 4);
+        r0 += (a.x > key) + (a.y > key) + (a.z > key) + (a.w > key);
+        r1 += (b.x > key) + (b.y > key) + (b.z > key) + (b.w > key);
+      }
+      rank = r0 + r1;
+    } else {
+      for (int e2 = 0; e2 < E; e2 += 4) {
+        const int4 c4 = *reinterpret_cast<const int4*>(sh.cnt + e2);
+        rank += (c4.x > run) || (c4.x == run && e2 < tid);
+        rank += (c4.y > run) || (c4.y == run && e2 + 1 < tid);
+        rank += (c4.z > run) || (c4.z == run && e2 + 2 < tid);
+        rank += (c4.w > run) || (c4.w == run && e2 + 3 < tid);
+      }
     }
     order[rank] = tid;
     sh.tiles[rank] = nbig;
