@@ -232,8 +232,9 @@ int run_quant(Ctx& c, const float* x, cudaStream_t st) {
                                   (__half*)c.v.xq, c.v.dx, st));
 }
 
-int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaStream_t st,
-             bool fuse_swiglu = false, const float* comb_w = nullptr, float* comb_out = nullptr) {
+GemmArgs gemm_args(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff,
+                   bool fuse_swiglu = false, const float* comb_w = nullptr,
+                   float* comb_out = nullptr) {
   GemmArgs a{};
   a.pack = pack;
   a.eoff = eoff;
@@ -272,6 +273,12 @@ int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaSt
       a.comb.k = c.d.k;
     }
   }
+  return a;
+}
+
+int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaStream_t st,
+             bool fuse_swiglu = false, const float* comb_w = nullptr, float* comb_out = nullptr) {
+  const GemmArgs a = gemm_args(c, which, pack, eoff, fuse_swiglu, comb_w, comb_out);
   // 128-row tiles on the tcgen05 kernel, short remainders on the small-row
   // tier (both read the tile list's split point on the device), the latter
   // on the side stream when there is one
@@ -288,6 +295,33 @@ int run_gemm(Ctx& c, int which, const uint8_t* pack, const int64_t* eoff, cudaSt
              cudaStreamWaitEvent(st, sd->join, 0) != cudaSuccess))
     return MOE_ERR_LAUNCH;
   return launch_rc(e2);
+}
+
+// Both product stages of the layer (gate/up with swiglu_quant fused, then
+// down), with one fork and one join: the tcgen05 launches run one after the
+// other on the caller's stream and the small-row launches on the side
+// stream.  A small-row tile's down product reads only the Hq rows that its
+// own gate/up launch wrote (every routed row is in one tile, and both stages
+// split the tile list at the same point), so neither chain waits for the
+// other before the join.
+int run_products(Ctx& c, const uint8_t* pack, const int64_t* eoff, cudaStream_t st,
+                 const float* comb_w = nullptr, float* comb_out = nullptr) {
+  const GemmArgs g = gemm_args(c, 0, pack, eoff, true);
+  const GemmArgs d = gemm_args(c, 1, pack, eoff, false, comb_w, comb_out);
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  SideStream* sd = side_stream(st);
+  if (sd && (cudaEventRecord(sd->fork, st) != cudaSuccess ||
+             cudaStreamWaitEvent(sd->s, sd->fork, 0) != cudaSuccess))
+    return MOE_ERR_LAUNCH;
+  cudaStream_t ss = sd ? sd->s : st;
+  cudaError_t e = launch_gemm_tc(g, st);
+  if (e == cudaSuccess) e = launch_gemm_small(g, ss);
+  if (e == cudaSuccess) e = launch_gemm_tc(d, st);
+  if (e == cudaSuccess) e = launch_gemm_small(d, ss);
+  if (sd && (cudaEventRecord(sd->join, sd->s) != cudaSuccess ||
+             cudaStreamWaitEvent(st, sd->join, 0) != cudaSuccess))
+    return MOE_ERR_LAUNCH;
+  return launch_rc(e);
 }
 
 int run_swiglu(Ctx& c, cudaStream_t st) {
@@ -310,12 +344,19 @@ int run_down_combine(Ctx& c, const uint8_t* pack, const int64_t* eoff, const flo
   return run_gemm(c, 1, pack, eoff, st, false, w, out);
 }
 
-// The layer's last two steps: down then combine, or both fused.
-int run_down_and_combine(Ctx& c, const uint8_t* pack, const int64_t* eoff, const float* w,
-                         float* out, cudaStream_t st) {
-  if (c.d.flags & MOE_FLAG_FUSED_COMBINE) return run_down_combine(c, pack, eoff, w, out, st);
-  int rc = run_gemm(c, 1, pack, eoff, st);
-  if (rc) return rc;
+// The layer after quant_q8: both products, then the combine (or, with
+// MOE_FLAG_FUSED_COMBINE, the combine inside the down epilogues, its arrival
+// counters set up first).
+int run_layer_tail(Ctx& c, const uint8_t* pack, const int64_t* eoff, const float* w, float* out,
+                   cudaStream_t st) {
+  int rc;
+  if (c.d.flags & MOE_FLAG_FUSED_COMBINE) {
+    if ((rc = launch_rc(launch_combine_init(c.v.dst_of, c.d.T, c.d.k, c.d.d / 32,
+                                            (int32_t*)(c.ws + c.L.cnt), st))))
+      return rc;
+    return run_products(c, pack, eoff, st, w, out);
+  }
+  if ((rc = run_products(c, pack, eoff, st))) return rc;
   return run_combine(c, w, out, st);
 }
 
@@ -470,8 +511,7 @@ int moe_prefill_layer(const MoeLayerDesc* desc, const float* x, const int32_t* t
   cudaStream_t st = (cudaStream_t)stream;
   if ((rc = run_route(c, topk_ids, st))) return rc;
   if ((rc = run_quant(c, x, st))) return rc;
-  if ((rc = run_gemm(c, 0, weight_pack, expert_offsets, st, true))) return rc;
-  return run_down_and_combine(c, weight_pack, expert_offsets, topk_w, out, st);
+  return run_layer_tail(c, weight_pack, expert_offsets, topk_w, out, st);
 }
 
 size_t moe_host_io_bytes(const MoeLayerDesc* desc) {
@@ -559,13 +599,12 @@ int moe_prefill_layer_host(const MoeLayerDesc* desc, const float* h_x, const int
     lock.unlock();
     if (!rec) return MOE_ERR_LAUNCH;
   }
-  if ((rc = run_gemm(c, 0, weight_pack, expert_offsets, st, true))) return rc;
   if (!overlap || (c.d.flags & MOE_FLAG_FUSED_COMBINE)) {
-    if ((rc = run_down_and_combine(c, weight_pack, expert_offsets, d_w, d_out, st))) return rc;
+    if ((rc = run_layer_tail(c, weight_pack, expert_offsets, d_w, d_out, st))) return rc;
     if (!ok(cudaMemcpyAsync(h_out, d_out, bx, cudaMemcpyDeviceToHost, st))) return MOE_ERR_LAUNCH;
     return MOE_OK;
   }
-  if ((rc = run_gemm(c, 1, weight_pack, expert_offsets, st))) return rc;
+  if ((rc = run_products(c, weight_pack, expert_offsets, st))) return rc;
   lock.lock();
   if (!ok(cudaStreamWaitEvent(st, sd->out_done, 0))) return MOE_ERR_LAUNCH;
   const size_t row_bytes = sizeof(float) * c.d.d;
