@@ -26,12 +26,14 @@
  *   - Every pointer argument named d_* or documented "device" is device
  *     memory of the current CUDA device, owned by the caller.  The library
  *     allocates no device memory and keeps no state between calls except a
- *     launch counter and, per device, one CUDA stream and two events
+ *     launch counter and, per device, three CUDA streams and seven events
  *     (created on the first product call that is not being captured, kept
- *     until the process exits): the products' small-row launch runs on that
+ *     until the process exits): the products' small-row launches run on one
  *     stream, forked from `stream` by an event and joined back before the
- *     call returns, so the work stays ordered on `stream` (under stream
- *     capture, as graph edges).  All work is enqueued with no host
+ *     call returns (once per stage in the stage entry points, once for both
+ *     products in the whole-layer calls), so the work stays ordered on
+ *     `stream` (under stream capture, as graph edges); the host-buffer
+ *     layer's copies run on the other two.  All work is enqueued with no host
  *     synchronisation, unless the entry point says otherwise.
  *   - Arguments are validated on the host before anything is launched; a
  *     negative MOE_ERR_* code is returned and nothing is enqueued.
