@@ -557,9 +557,10 @@ __device__ __forceinline__ ItemInfo item_info(const SmArgs& a, int first, int n_
 // the last CTA to finish zeroes them again for the next launch.
 //
 // The load side of the ring (run by whichever warp releases a slot last):
-// the next (item, chunk) to load, in the order the warps consume them.  Per chunk: one bulk copy of
-// the raw weight chunk and the tile's activation rows and scales in 2-D TMA
-// boxes of 16 rows (rows past the tile land in rows that are never read).
+// the next (item, chunk) to load, in the order the warps consume them.  Per
+// chunk: one bulk copy of the raw weight chunk and the tile's activation
+// rows and scales in 2-D TMA boxes of 16 rows (rows past the tile land in
+// rows that are never read).
 struct Producer {
   int item, c;  // next item (>= total: nothing left) and chunk
   const uint8_t* wbase;
