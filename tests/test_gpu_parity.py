@@ -696,6 +696,9 @@ def test_host_buffers_deferred_out(M):
     torch.cuda.synchronize()
     for ho, ref in zip(outs, refs):
         assert np.array_equal(ho.numpy(), ref)
+    # nothing pending: the join enqueues a wait on a completed copy
+    M.moe_host_out_join()
+    torch.cuda.synchronize()
 
 
 def test_host_buffers_fewer_tokens_than_chunks(M):
