@@ -263,8 +263,10 @@ int moe_prefill_layer(const MoeLayerDesc *desc, const float *x,
  *
  * moe_host_out_join makes `stream` wait for every out copy that host-buffer
  * calls on the current device have enqueued so far (MOE_OK and nothing
- * enqueued when there is none); with MOE_FLAG_HOST_OUT_DEFERRED the caller
- * enqueues it, then synchronises `stream`, before reading any h_out. */
+ * enqueued when there is none, or when `stream` is being captured: there
+ * the copies run on the stream in order); with MOE_FLAG_HOST_OUT_DEFERRED
+ * the caller enqueues it, then synchronises `stream`, before reading any
+ * h_out. */
 size_t moe_host_io_bytes(const MoeLayerDesc *desc);
 int moe_prefill_layer_host(const MoeLayerDesc *desc, const float *h_x,
                            const int32_t *h_topk_ids, const float *h_topk_w,

@@ -568,8 +568,12 @@ int moe_prefill_layer_host(const MoeLayerDesc* desc, const float* h_x, const int
     if ((rc = run_route(c, d_ids, st))) return rc;
     return MOE_OK;
   }
+  // under stream capture every copy runs on `stream` in order: the copy
+  // streams' events from earlier calls lie outside the capture
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return MOE_ERR_LAUNCH;
   std::unique_lock<std::mutex> lock(g_side_mu);
-  SideStream* sd = side_stream(st);
+  SideStream* sd = cs == cudaStreamCaptureStatusNone ? side_stream(st) : nullptr;
   const bool overlap = sd != nullptr;
   auto ok = [](cudaError_t e) { return e == cudaSuccess; };
   if (overlap) {
@@ -629,6 +633,11 @@ int moe_prefill_layer_host(const MoeLayerDesc* desc, const float* h_x, const int
 int moe_host_out_join(moe_stream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_DEVICE;
+  // a stream being captured copies out in order itself (no copy streams), and
+  // may not wait on an event recorded outside the capture
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing((cudaStream_t)stream, &cs) != cudaSuccess) return MOE_ERR_LAUNCH;
+  if (cs != cudaStreamCaptureStatusNone) return MOE_OK;
   std::lock_guard<std::mutex> lock(g_side_mu);
   const SideStream& sd = g_side[dev];
   if (sd.ctx != current_context_id() || !sd.out_pending) return MOE_OK;

@@ -701,6 +701,37 @@ def test_host_buffers_deferred_out(M):
     torch.cuda.synchronize()
 
 
+def test_host_buffers_captured_in_a_graph(M):
+    """The host-buffer layer captured in a CUDA graph after an ordinary call
+    (its copy streams exist by then), with MOE_FLAG_HOST_OUT_DEFERRED and the
+    join: under capture every copy runs on the capturing stream in order,
+    and each replay gives the device entry's out bit for bit."""
+    L = SMALL["mid_w2_w2"]()
+    dl = DeviceLayer(M, L)
+    dl.run_layer()
+    ref = dl.out.cpu().numpy()
+    hx = torch.from_numpy(L.x).pin_memory()
+    hi = torch.from_numpy(L.topk_ids).pin_memory()
+    hw = torch.from_numpy(L.topk_w).pin_memory()
+    ho = torch.empty((L.shape.T, L.shape.d), dtype=torch.float32).pin_memory()
+    io = torch.empty(M.host_io_bytes(dl.desc), dtype=torch.uint8, device="cuda")
+    desc = type(dl.desc).from_buffer_copy(dl.desc)
+    desc.flags = M.MOE_FLAG_HOST_OUT_DEFERRED
+    M.moe_prefill_layer_host(desc, hx, hi, hw, dl.pack, dl.eoff, ho, io, dl.ws)
+    M.moe_host_out_join()
+    torch.cuda.synchronize()
+    assert np.array_equal(ho.numpy(), ref)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        M.moe_prefill_layer_host(desc, hx, hi, hw, dl.pack, dl.eoff, ho, io, dl.ws)
+        M.moe_host_out_join()
+    for _ in range(2):
+        ho.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(ho.numpy(), ref)
+
+
 def test_host_buffers_fewer_tokens_than_chunks(M):
     """The host-buffer layer at T = 5 (some token chunks of its combine and
     out copy are empty) equals the device entry."""
