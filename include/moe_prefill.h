@@ -158,7 +158,9 @@ typedef struct MoeLayerDesc {
  *                            sd = d/32 rounded up to a multiple of 4
  *   gu      fp32  [R*2*n_ff] gate/up rows, columns in the weight rows' order:
  *                            gate j at j and up j at n_ff+j (MOE_GU_SPLIT)
- *                            or at 2j and 2j+1 (MOE_GU_INTERLEAVED)
+ *                            or at 2j and 2j+1 (MOE_GU_INTERLEAVED); the
+ *                            same bytes as dm (gu == dm): the down product
+ *                            overwrites it, the fused layer never writes it
  *   hq      fp16  [R*n_ff]   q8 values of H as exact fp16 integers, stored
  *                            pair-interleaved like xq
  *   dh      fp32  [R*sf]     q8 scales of H, rows padded to sf = n_ff/32

@@ -92,10 +92,12 @@ Layout layout(const MoeLayerDesc& d) {
   L.hist = take(sizeof(int32_t) * (size_t)route_hist_rows(R) * d.E);
   L.xq = take(sizeof(uint16_t) * (size_t)R * d.d);
   L.dx = take(sizeof(float) * (size_t)R * scale_stride(d.d));
-  L.gu = take(sizeof(float) * (size_t)R * 2 * d.n_ff);
   L.hq = take(sizeof(uint16_t) * (size_t)R * d.n_ff);
   L.dh = take(sizeof(float) * (size_t)R * scale_stride(d.n_ff));
-  L.dm = take(sizeof(float) * (size_t)R * d.d);
+  // gu lives from the gate/up product to swiglu_quant (the whole layer never
+  // writes it), dm from the down product to the combine: one region for both
+  L.dm = take(sizeof(float) * (size_t)R * std::max(d.d, 2 * d.n_ff));
+  L.gu = L.dm;
   L.cnt = take(sizeof(int32_t) * (size_t)d.T * (d.d / 32));  // fused combine's counters
   L.total = p;
   return L;

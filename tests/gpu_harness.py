@@ -91,6 +91,7 @@ class DeviceLayer:
         self.ws = M.alloc_workspace(self.desc)
         self.ws.fill_(0xFF)  # poison: nothing may rely on zeroed workspace
         self.v = M.workspace_view(self.desc, self.ws)
+        self.gu_copy = None  # gu as the stage sequence left it (dm overwrites it)
 
     def run_layer(self):
         """The whole layer (gate/up with swiglu_quant fused: gu is not written)."""
@@ -98,6 +99,7 @@ class DeviceLayer:
                                  self.out, self.ws)
         torch.cuda.synchronize()
         self.has_gu = False
+        self.gu_copy = None
 
     def run_stages(self):
         M = self.M
@@ -105,6 +107,8 @@ class DeviceLayer:
         M.moe_quant_q8(self.desc, self.x, self.ws)
         M.moe_gate_up(self.desc, self.pack, self.eoff, self.ws)
         M.moe_swiglu_quant(self.desc, self.ws)
+        # gu shares its bytes with dm, which the down product overwrites
+        self.gu_copy = self.v["gu"].clone()
         M.moe_down(self.desc, self.pack, self.eoff, self.ws)
         M.moe_combine(self.desc, self.w, self.out, self.ws)
         torch.cuda.synchronize()
@@ -116,7 +120,7 @@ class DeviceLayer:
     def get(self, name, rows=None) -> np.ndarray:
         """A workspace region as numpy, in natural order: q8 values
         un-interleaved, scale rows without their padding."""
-        t = self.v[name]
+        t = self.gu_copy if name == "gu" and self.gu_copy is not None else self.v[name]
         if name == "dx":
             t = t[:, : self.L.shape.d // 32]
         if name == "dh":

@@ -43,11 +43,28 @@ def test_workspace_bytes_layout(lib):
     d = M.make_desc(16384, 2560, 640, 512, 10)
     n = M.workspace_bytes(d)
     R = 16384 * 10
-    # per routed row: gu, hq, dh, dm, row_src + dst_of, scattered xq and dx
-    minimum = R * (2 * 640 * 4 + 640 * 2 + 20 * 4 + 2560 * 4 + 8 + 2560 * 2 + 80 * 4)
+    # per routed row: hq, dh, dm (which gu shares), row_src + dst_of,
+    # scattered xq and dx
+    minimum = R * (640 * 2 + 20 * 4 + 2560 * 4 + 8 + 2560 * 2 + 80 * 4)
     assert minimum <= n <= minimum + 64 * 2**20
     assert n % 256 == 0
     assert M.host_io_bytes(d) >= 2 * 16384 * 2560 * 4
+
+
+@pytest.mark.parametrize("d,n_ff", [(2560, 640), (256, 1024)])
+def test_gu_shares_the_dm_region(lib, d, n_ff):
+    """gu (live from the gate/up product to swiglu_quant) and dm (from the
+    down product to the combine) are one region, as large as the larger."""
+    desc = M.make_desc(64, d, n_ff, 8, 2)
+    need = lib.moe_prefill_workspace_bytes(ctypes.byref(desc))
+    base = 1 << 40  # never dereferenced: the view is host arithmetic
+    v = M.MoeWorkspaceView()
+    assert lib.moe_workspace_view(ctypes.byref(desc), ctypes.c_void_p(base), need,
+                                  ctypes.byref(v)) == 0
+    gu = ctypes.cast(v.gu, ctypes.c_void_p).value
+    dm = ctypes.cast(v.dm, ctypes.c_void_p).value
+    assert gu == dm
+    assert dm + 64 * 2 * max(d, 2 * n_ff) * 4 <= base + need
 
 
 @pytest.mark.parametrize("field,value,code", [
